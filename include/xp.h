@@ -1,0 +1,193 @@
+/*
+ * xp.h -- C ABI of the GB300 (sm_103a) XPress Jacobi refinement pass.
+ *
+ * One pass over a batch of N draft blocks of B slots (slot 0 = the verified
+ * anchor) computes, for every slot b:
+ *   latent   x[b] = xh[b] + W_lat w1[prev[b]],  prev[0] = am1, prev[b] = blk[b-1]
+ *            u[b] = sum_{j<=b} mix[c,b,j] x[j]  (per channel c, folded mixer)
+ *            lat[b] = u[b] + W_down (silu(W_gate u[b]) * (W_up u[b]))
+ *   readout  logits[b, v] = base[b, v] + lat[b] . w2[v]
+ *   argmax   blk[b] = argmax_v logits[b, v], written in place for the next pass
+ * for the draft slots b = 1..B-1, and repeats that K times (Jacobi iteration).
+ *
+ * Sources: the vLLM API page of vllm.model_executor.models.qwen3_xpress
+ * ("qwen3_xpress page": XPressRefinerHead and its methods) and the vLLM API
+ * page of vllm.v1.worker.gpu.spec_decode.xpress.kernels ("xpress kernels
+ * page": the docstrings of the per-pass kernels).
+ *
+ * Conventions (all entry points):
+ *  - Memory is owned by the caller.  The library never allocates device
+ *    memory; pointers marked "device" must be device (or managed) memory,
+ *    pointers marked "host" host memory.  Sizes are element counts unless
+ *    stated otherwise.
+ *  - Every call is asynchronous on the given stream (0 = legacy default) and
+ *    performs no host synchronisation, except xp_get_error and
+ *    xp_head_create/xp_head_refill (which synchronise nothing either, but
+ *    read device properties).  Host-side validation runs before any launch;
+ *    a call that returns an error has launched nothing.
+ *  - Token ids are int64 at the boundary.  A token id outside [0, V) read by
+ *    a kernel is clamped into range and raises XP_EBADTOKEN in the head's
+ *    device error word (read with xp_get_error); kernels never trap.
+ *  - Dtypes: the head's weights, base logits, h and latents all share the
+ *    head dtype (XP_BF16 or XP_F32); accumulation is fp32 throughout.
+ *  - Argmax ties go to the lowest vocabulary id (full vocabulary, init and
+ *    top-C alike); -0 compares equal to +0.  Inputs are assumed finite.
+ */
+#ifndef XP_H_
+#define XP_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  XP_OK = 0,
+  XP_EINVAL = 1,        /* null pointer, bad shape, bad stride or alignment            */
+  XP_ECAPACITY = 2,     /* N above the head's max_N, or a buffer too small             */
+  XP_ENOTPREPARED = 3,  /* head missing (the weights were never prepared)              */
+  XP_ECUDA = 4,         /* a CUDA runtime call failed (launch, copy, attribute)        */
+  XP_EBADTOKEN = 5,     /* device flag: a token id outside [0, V) was clamped          */
+  XP_ETIMEOUT = 6,      /* device flag: a bounded wait inside a kernel gave up         */
+  XP_EUNSUPPORTED = 7   /* shape not supported by this build                           */
+} xp_status;
+
+typedef enum { XP_BF16 = 0, XP_F32 = 1 } xp_dtype;
+
+/* Head weights, torch layouts ([out, in] row-major for linear maps).  All
+ * pointers are device pointers, read only during xp_head_create /
+ * xp_head_refill (they are copied into the head's prepared memory).
+ * qwen3_xpress page, XPressRefinerHead.__init__. */
+typedef struct {
+  int V;          /* vocabulary size                                   */
+  int hidden;     /* target-model hidden size                          */
+  int r;          /* refiner rank (latent width)                       */
+  int H;          /* SwiGLU hidden size (mlp_hidden)                   */
+  int B;          /* block size (slots per draft block, >= 2)          */
+  int max_N;      /* most blocks any call will pass (max_num_reqs)     */
+  xp_dtype dtype; /* storage type of every tensor below                */
+  const void* w1;       /* [V, r]       token embedding                     */
+  const void* down_h;   /* [r, hidden]                                      */
+  const void* down_g;   /* [r, hidden]                                      */
+  const void* in_proj;  /* [r, 3r]      columns: down_h | down_g | embedding */
+  const void* mix_L;    /* [r, B, B]    FOLDED mixer (raw*tril + I), index  */
+                        /*              [channel, out slot, in slot]        */
+  const void* w_gate;   /* [H, r]                                           */
+  const void* w_up;     /* [H, r]                                           */
+  const void* w_down;   /* [r, H]                                           */
+  const void* w2;       /* [V, r]       readout                             */
+} xp_weights;
+
+typedef struct xp_head xp_head; /* opaque, host-side */
+
+/* Device bytes the head's prepared copies need (caller allocates them once). */
+size_t xp_head_prep_bytes(const xp_weights* w);
+
+/* Device bytes of the per-call workspace for up to N blocks; topc > 0 adds
+ * the candidate buffers of the top-C path (cand, base_c, w2c) for C = topc. */
+size_t xp_workspace_bytes(const xp_weights* w, int N, int topc);
+
+/* Zero a workspace once after allocating it.  The argmax finish keeps its
+ * counters at zero between calls; after XP_ETIMEOUT, zero it again. */
+xp_status xp_workspace_init(void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Copy and lay out the weights into prep_dev (device, prep_bytes >=
+ * xp_head_prep_bytes) and return a host handle.  qwen3_xpress page,
+ * process_weights_after_loading: prepared copies the kernels index directly. */
+xp_status xp_head_create(const xp_weights* w, void* prep_dev, size_t prep_bytes,
+                         cudaStream_t stream, xp_head** out);
+
+/* Refill the prepared copies in place from new weights of the same shapes, so
+ * that captured CUDA graphs keep their addresses (process_weights_after_loading
+ * on a reload). */
+xp_status xp_head_refill(xp_head* head, const xp_weights* w, cudaStream_t stream);
+
+void xp_head_destroy(xp_head* head);
+
+/* mix_L[c,b,j] = raw_L[c,b,j] * [j <= b] + [j == b], evaluated in fp64 and
+ * rounded once to dtype.  raw_L, mix_L: device [r, B, B].
+ * qwen3_xpress page, XPressRefinerHead.fold_from_raw_. */
+xp_status xp_fold_mix(const void* raw_L, void* mix_L, int r, int B, xp_dtype dtype,
+                      cudaStream_t stream);
+
+/* Pass-invariant hidden half of in_proj, once per draft step:
+ *   xh[n,b] = in_proj[:, :2r] . [down_h h[n,b] ; down_g mean_b' h[n,b']]
+ * h_full: device [N, B, hidden] (head dtype); xh: device [N, B, r] fp32.
+ * ws: workspace of xp_workspace_bytes(w, >= N, *).
+ * qwen3_xpress page, hidden_cache and the xh hoist in jacobi_refine_greedy. */
+xp_status xp_hidden_cache(const xp_head* head, const void* h_full, int N, float* xh,
+                          void* ws, cudaStream_t stream);
+
+/* Latent stage of one pass (all slots), written for slots 1..B-1:
+ * blk: device [N, B] int64; am1: device [N] int64; xh: device [N, B, r] fp32;
+ * lat: device [N, B-1, r] head dtype (written).
+ * xpress kernels page, _xpress_latent_kernel; qwen3_xpress page, _refine_latent. */
+xp_status xp_latent_pass(const xp_head* head, const int64_t* blk, const int64_t* am1,
+                         const float* xh, int N, void* lat, cudaStream_t stream);
+
+/* Readout + argmax straight into the block:
+ *   blk[n, 1+b] = argmax_v (base[n,b,v] + lat[n,b] . w2[v]),  b = 0..B-2
+ * lat: device [N, B-1, r] head dtype.  base: device, draft row (n, b) starts
+ * at base + n*stride_n + b*stride_b (elements), unit stride over v.  blk:
+ * device [N, B] int64, slots 1..B-1 written.  win_val: device [N*(B-1)]
+ * fp32 winning logits, or NULL.  ws: workspace (argmax partials).
+ * The [N*(B-1), V] logits are never written to memory.
+ * xpress kernels page, fused_add_argmax_to_blk; qwen3_xpress page, refine_bias. */
+xp_status xp_readout_argmax(const xp_head* head, const void* lat, const void* base,
+                            int64_t stride_n, int64_t stride_b, int N, int64_t* blk,
+                            float* win_val, void* ws, cudaStream_t stream);
+
+/* Initial block: blk[n,0] = anchor[n], blk[n,1+b] = argmax_v base[n,b,v].
+ * Same base addressing as xp_readout_argmax.  anchor: device [N] int64.
+ * qwen3_xpress page, jacobi_refine_greedy (before the passes). */
+xp_status xp_init_argmax(const xp_head* head, const void* base, int64_t stride_n,
+                         int64_t stride_b, const int64_t* anchor, int N, int64_t* blk,
+                         float* win_val, void* ws, cudaStream_t stream);
+
+/* Top-C candidates, once per draft step.  Per draft row: the C largest base
+ * values (ties at the boundary to the lower id), stored in ascending id order:
+ * cand: device [N, B-1, C] int64; base_c: device [N, B-1, C] head dtype;
+ * w2c: device [N, B-1, C, r] head dtype = w2[cand] rows, or NULL to have the
+ * top-C readout gather w2 rows itself each pass.  blk: device [N, B] int64 or
+ * NULL; when given, slots 1..B-1 receive the base argmax (the init).
+ * 1 <= C <= V.  qwen3_xpress page, jacobi_refine_greedy top-C branch. */
+xp_status xp_topc_gather(const xp_head* head, const void* base, int64_t stride_n,
+                         int64_t stride_b, int N, int C, int64_t* cand, void* base_c,
+                         void* w2c, int64_t* blk, cudaStream_t stream);
+
+/* Top-C readout + argmax, per pass:
+ *   blk[n, 1+b] = cand[n,b,k*],  k* = argmax_k (base_c[n,b,k] + w2c[n,b,k] . lat[n,b])
+ * ties to the lowest vocabulary id.  w2c may be NULL (rows gathered from the
+ * head's w2 through cand).  win_val: device [N*(B-1)] fp32 or NULL.
+ * xpress kernels page, _xpress_topc_argmax_to_blk_kernel. */
+xp_status xp_topc_readout_argmax(const xp_head* head, const void* lat, const void* base_c,
+                                 const int64_t* cand, const void* w2c, int N, int C,
+                                 int64_t* blk, float* win_val, cudaStream_t stream);
+
+/* Whole draft step: hidden cache, init argmax (or top-C gather when topc > 0),
+ * then K passes of latent + readout-argmax.  blk: device [N, B] int64 (out;
+ * slot 0 = anchor).  topc >= V scores the full vocabulary through the top-C
+ * path with C = V.  ws: workspace of xp_workspace_bytes(w, >= N, topc).
+ * qwen3_xpress page, XPressRefinerHead.jacobi_refine_greedy. */
+xp_status xp_jacobi_refine(const xp_head* head, const void* base, int64_t stride_n,
+                           int64_t stride_b, const void* h_full, const int64_t* anchor,
+                           const int64_t* am1, int N, int K, int topc, int64_t* blk,
+                           void* ws, cudaStream_t stream);
+
+/* Synchronise `stream`, read and clear the head's device error word:
+ * XP_OK, XP_EBADTOKEN or XP_ETIMEOUT (timeout wins when both are set). */
+xp_status xp_get_error(const xp_head* head, cudaStream_t stream);
+
+/* Name of the readout kernel the head uses for its shape (for profiling). */
+const char* xp_readout_kernel_name(const xp_head* head);
+
+const char* xp_status_str(xp_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* XP_H_ */

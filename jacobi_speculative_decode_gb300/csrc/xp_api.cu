@@ -1,0 +1,383 @@
+// Host side of the C ABI: validation, prepared weight copies, workspace layout
+// and the order of launches.  Every compute step runs in the kernels.
+#include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+#include <new>
+
+#include "xp_internal.h"
+
+namespace {
+
+constexpr size_t kAlign = 1024;
+inline size_t align_up(size_t x, size_t a = kAlign) { return (x + a - 1) / a * a; }
+
+bool valid_weights(const xp_weights* w) {
+  if (!w) return false;
+  if (w->V <= 0 || w->hidden <= 0 || w->r <= 0 || w->H <= 0 || w->B < 2 || w->max_N <= 0)
+    return false;
+  if (w->B > 64) return false;   // the latent kernels keep a block's slots on chip
+  if (w->dtype != XP_BF16 && w->dtype != XP_F32) return false;
+  return true;
+}
+
+bool valid_weight_ptrs(const xp_weights* w) {
+  return w->w1 && w->down_h && w->down_g && w->in_proj && w->mix_L && w->w_gate && w->w_up &&
+         w->w_down && w->w2;
+}
+
+struct PrepLayout {
+  size_t err, w1, down_h, down_g, w_hc, w_lat, mix, w_gate, w_up, w_down, w2, total;
+};
+
+PrepLayout prep_layout(const xp_weights* w) {
+  const size_t es = xp_elem(w->dtype);
+  const size_t V = w->V, r = w->r, H = w->H, hid = w->hidden, B = w->B;
+  PrepLayout L;
+  size_t o = 0;
+  auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes); return at; };
+  L.err = take(256);
+  L.w1 = take(V * r * es);
+  L.down_h = take(r * hid * es);
+  L.down_g = take(r * hid * es);
+  L.w_hc = take(r * 2 * r * es);
+  L.w_lat = take(r * r * es);
+  L.mix = take(r * B * B * es);
+  L.w_gate = take(H * r * es);
+  L.w_up = take(H * r * es);
+  L.w_down = take(r * H * es);
+  L.w2 = take(V * r * es);
+  L.total = o;
+  return L;
+}
+
+xp_status copy_weights(xp_head* h, const xp_weights* w, cudaStream_t s) {
+  const size_t es = xp_elem(w->dtype);
+  const size_t V = w->V, r = w->r, H = w->H, hid = w->hidden, B = w->B;
+  cudaError_t e = cudaSuccess;
+  auto cp = [&](void* dst, const void* src, size_t bytes) {
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, s);
+  };
+  cp(h->w1, w->w1, V * r * es);
+  cp(h->down_h, w->down_h, r * hid * es);
+  cp(h->down_g, w->down_g, r * hid * es);
+  // in_proj [r, 3r]: columns [0, 2r) act on the hidden cache, [2r, 3r) on the embedding
+  if (e == cudaSuccess)
+    e = cudaMemcpy2DAsync(h->w_hc, 2 * r * es, w->in_proj, 3 * r * es, 2 * r * es, r,
+                          cudaMemcpyDeviceToDevice, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpy2DAsync(h->w_lat, r * es, (const char*)w->in_proj + 2 * r * es, 3 * r * es,
+                          r * es, r, cudaMemcpyDeviceToDevice, s);
+  cp(h->mix, w->mix_L, r * B * B * es);
+  cp(h->w_gate, w->w_gate, H * r * es);
+  cp(h->w_up, w->w_up, H * r * es);
+  cp(h->w_down, w->w_down, r * H * es);
+  cp(h->w2, w->w2, V * r * es);
+  return e == cudaSuccess ? XP_OK : XP_ECUDA;
+}
+
+inline xp_status cuda_status(cudaError_t e) { return e == cudaSuccess ? XP_OK : XP_ECUDA; }
+
+bool valid_base(const xp_head* h, const void* base, int64_t sn, int64_t sb) {
+  return base && sn >= 0 && sb >= 0;
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+xp_ws_layout xp_layout(int V, int hidden, int r, int B, int max_N, xp_dtype dt, int N, int C) {
+  (void)V;
+  const size_t es = xp_elem(dt);
+  const size_t rows_cap = (size_t)max_N * (B - 1);
+  xp_ws_layout L;
+  size_t o = 0;
+  auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes); return at; };
+  L.ro_packed = take(rows_cap * 8);
+  L.ro_ticket = take(rows_cap * 4);
+  L.in_packed = take(rows_cap * 8);
+  L.in_ticket = take(rows_cap * 4);
+  L.zero_end = o;
+  L.xh = take((size_t)max_N * B * r * 4);
+  L.lat = take(rows_cap * r * es);
+  L.hmean = take((size_t)max_N * hidden * 4);
+  L.hc = take((size_t)max_N * B * 2 * r * 4);
+  L.hcg = take((size_t)max_N * r * 4);
+  const size_t rows = (size_t)std::max(N, 0) * (B - 1);
+  const size_t c = (size_t)std::max(C, 0);
+  L.cand = take(rows * c * 8);
+  L.base_c = take(rows * c * es);
+  L.w2c = take(rows * c * r * es);
+  L.total = o;
+  return L;
+}
+
+extern "C" {
+
+const char* xp_status_str(xp_status s) {
+  switch (s) {
+    case XP_OK: return "ok";
+    case XP_EINVAL: return "invalid argument";
+    case XP_ECAPACITY: return "capacity exceeded";
+    case XP_ENOTPREPARED: return "head not prepared";
+    case XP_ECUDA: return "CUDA runtime error";
+    case XP_EBADTOKEN: return "token id out of range (clamped)";
+    case XP_ETIMEOUT: return "bounded wait in a kernel timed out";
+    case XP_EUNSUPPORTED: return "unsupported shape";
+  }
+  return "unknown status";
+}
+
+size_t xp_head_prep_bytes(const xp_weights* w) {
+  if (!valid_weights(w)) return 0;
+  return prep_layout(w).total;
+}
+
+size_t xp_workspace_bytes(const xp_weights* w, int N, int topc) {
+  if (!valid_weights(w) || N < 0 || topc < 0) return 0;
+  const int C = topc > 0 ? std::min(topc, w->V) : 0;
+  return xp_layout(w->V, w->hidden, w->r, w->B, w->max_N, w->dtype, N, C).total;
+}
+
+xp_status xp_workspace_init(void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (!ws || ws_bytes == 0) return XP_EINVAL;
+  return cuda_status(cudaMemsetAsync(ws, 0, ws_bytes, stream));
+}
+
+static void decide_paths(xp_head* h);
+
+xp_status xp_head_create(const xp_weights* w, void* prep_dev, size_t prep_bytes,
+                         cudaStream_t stream, xp_head** out) {
+  if (!out) return XP_EINVAL;
+  *out = nullptr;
+  if (!valid_weights(w) || !valid_weight_ptrs(w) || !prep_dev) return XP_EINVAL;
+  if ((uintptr_t)prep_dev % 256 != 0) return XP_EINVAL;
+  const PrepLayout L = prep_layout(w);
+  if (prep_bytes < L.total) return XP_ECAPACITY;
+  xp_head* h = new (std::nothrow) xp_head();
+  if (!h) return XP_ECAPACITY;
+  h->V = w->V; h->hidden = w->hidden; h->r = w->r; h->H = w->H; h->B = w->B;
+  h->max_N = w->max_N; h->dtype = w->dtype;
+  h->prep = (char*)prep_dev;
+  h->prep_bytes = prep_bytes;
+  if (cudaGetDevice(&h->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device) !=
+          cudaSuccess) {
+    delete h;
+    return XP_ECUDA;
+  }
+  char* p = h->prep;
+  h->err = (uint32_t*)(p + L.err);
+  h->w1 = p + L.w1; h->down_h = p + L.down_h; h->down_g = p + L.down_g;
+  h->w_hc = p + L.w_hc; h->w_lat = p + L.w_lat; h->mix = p + L.mix;
+  h->w_gate = p + L.w_gate; h->w_up = p + L.w_up; h->w_down = p + L.w_down; h->w2 = p + L.w2;
+  xp_status st = copy_weights(h, w, stream);
+  if (st == XP_OK) st = cuda_status(cudaMemsetAsync(h->err, 0, 256, stream));
+  if (st != XP_OK) { delete h; return st; }
+  decide_paths(h);
+  *out = h;
+  return XP_OK;
+}
+
+xp_status xp_head_refill(xp_head* h, const xp_weights* w, cudaStream_t stream) {
+  if (!h) return XP_ENOTPREPARED;
+  if (!valid_weights(w) || !valid_weight_ptrs(w)) return XP_EINVAL;
+  if (w->V != h->V || w->hidden != h->hidden || w->r != h->r || w->H != h->H || w->B != h->B ||
+      w->dtype != h->dtype || w->max_N != h->max_N)
+    return XP_EINVAL;
+  return copy_weights(h, w, stream);
+}
+
+void xp_head_destroy(xp_head* h) { delete h; }
+
+xp_status xp_fold_mix(const void* raw_L, void* mix_L, int r, int B, xp_dtype dtype,
+                      cudaStream_t stream) {
+  if (!raw_L || !mix_L || r <= 0 || B <= 0 || (dtype != XP_BF16 && dtype != XP_F32))
+    return XP_EINVAL;
+  return cuda_status(xp_launch_fold(raw_L, mix_L, r, B, dtype, stream));
+}
+
+xp_status xp_hidden_cache(const xp_head* h, const void* h_full, int N, float* xh, void* ws,
+                          cudaStream_t stream) {
+  if (!h) return XP_ENOTPREPARED;
+  if (!h_full || !xh || !ws || N < 0) return XP_EINVAL;
+  if (N > h->max_N) return XP_ECAPACITY;
+  if (N == 0) return XP_OK;
+  const xp_ws_layout L = xp_layout(h->V, h->hidden, h->r, h->B, h->max_N, h->dtype, N, 0);
+  char* w = (char*)ws;
+  return cuda_status(xp_launch_hidden(h, h_full, N, xh, (float*)(w + L.hmean), (float*)(w + L.hc),
+                                      (float*)(w + L.hcg), stream));
+}
+
+xp_status xp_latent_pass(const xp_head* h, const int64_t* blk, const int64_t* am1,
+                         const float* xh, int N, void* lat, cudaStream_t stream) {
+  if (!h) return XP_ENOTPREPARED;
+  if (!blk || !am1 || !xh || !lat || N < 0) return XP_EINVAL;
+  if (N > h->max_N) return XP_ECAPACITY;
+  if (N == 0) return XP_OK;
+  if (h->latent_mma) return cuda_status(xp_launch_latent_mma(h, blk, am1, xh, N, lat, stream));
+  return cuda_status(xp_launch_latent_simt(h, blk, am1, xh, N, lat, stream));
+}
+
+static xp_status readout_impl(const xp_head* h, const void* lat, const void* base, int64_t sn,
+                              int64_t sb, int N, int64_t* blk, float* win, void* ws,
+                              cudaStream_t stream) {
+  const xp_ws_layout L = xp_layout(h->V, h->hidden, h->r, h->B, h->max_N, h->dtype, N, 0);
+  char* w = (char*)ws;
+  auto* packed = (unsigned long long*)(w + L.ro_packed);
+  auto* ticket = (unsigned*)(w + L.ro_ticket);
+  if (h->readout_tc && xp_readout_tc_call_ok(h, lat, base, sn, sb, N))
+    return cuda_status(
+        xp_launch_readout_tc(h, lat, base, sn, sb, N, blk, win, packed, ticket, stream));
+  return cuda_status(
+      xp_launch_readout_simt(h, lat, base, sn, sb, N, blk, win, packed, ticket, stream));
+}
+
+xp_status xp_readout_argmax(const xp_head* h, const void* lat, const void* base, int64_t sn,
+                            int64_t sb, int N, int64_t* blk, float* win, void* ws,
+                            cudaStream_t stream) {
+  if (!h) return XP_ENOTPREPARED;
+  if (!lat || !valid_base(h, base, sn, sb) || !blk || !ws || N < 0) return XP_EINVAL;
+  if (N > h->max_N) return XP_ECAPACITY;
+  if (N == 0) return XP_OK;
+  return readout_impl(h, lat, base, sn, sb, N, blk, win, ws, stream);
+}
+
+xp_status xp_init_argmax(const xp_head* h, const void* base, int64_t sn, int64_t sb,
+                         const int64_t* anchor, int N, int64_t* blk, float* win, void* ws,
+                         cudaStream_t stream) {
+  if (!h) return XP_ENOTPREPARED;
+  if (!valid_base(h, base, sn, sb) || !anchor || !blk || !ws || N < 0) return XP_EINVAL;
+  if (N > h->max_N) return XP_ECAPACITY;
+  if (N == 0) return XP_OK;
+  const xp_ws_layout L = xp_layout(h->V, h->hidden, h->r, h->B, h->max_N, h->dtype, N, 0);
+  char* w = (char*)ws;
+  return cuda_status(xp_launch_init_argmax(h, base, sn, sb, anchor, N, blk, win,
+                                           (unsigned long long*)(w + L.in_packed),
+                                           (unsigned*)(w + L.in_ticket), stream));
+}
+
+xp_status xp_topc_gather(const xp_head* h, const void* base, int64_t sn, int64_t sb, int N, int C,
+                         int64_t* cand, void* base_c, void* w2c, int64_t* blk,
+                         cudaStream_t stream) {
+  if (!h) return XP_ENOTPREPARED;
+  if (!valid_base(h, base, sn, sb) || !cand || !base_c || N < 0 || C < 1 || C > h->V)
+    return XP_EINVAL;
+  if (N > h->max_N) return XP_ECAPACITY;
+  if (N == 0) return XP_OK;
+  return cuda_status(
+      xp_launch_topc_gather(h, base, sn, sb, N, C, cand, base_c, w2c, blk, nullptr, stream));
+}
+
+xp_status xp_topc_readout_argmax(const xp_head* h, const void* lat, const void* base_c,
+                                 const int64_t* cand, const void* w2c, int N, int C, int64_t* blk,
+                                 float* win, cudaStream_t stream) {
+  if (!h) return XP_ENOTPREPARED;
+  if (!lat || !base_c || !cand || !blk || N < 0 || C < 1 || C > h->V) return XP_EINVAL;
+  if (N > h->max_N) return XP_ECAPACITY;
+  if (N == 0) return XP_OK;
+  return cuda_status(xp_launch_topc_readout(h, lat, base_c, cand, w2c, N, C, blk, win, stream));
+}
+
+xp_status xp_jacobi_refine(const xp_head* h, const void* base, int64_t sn, int64_t sb,
+                           const void* h_full, const int64_t* anchor, const int64_t* am1, int N,
+                           int K, int topc, int64_t* blk, void* ws, cudaStream_t stream) {
+  if (!h) return XP_ENOTPREPARED;
+  if (!valid_base(h, base, sn, sb) || !h_full || !anchor || !am1 || !blk || !ws || N < 0 ||
+      K < 0 || topc < 0)
+    return XP_EINVAL;
+  if (N > h->max_N) return XP_ECAPACITY;
+  if (N == 0) return XP_OK;
+  const int C = topc > 0 ? std::min(topc, h->V) : 0;
+  const xp_ws_layout L = xp_layout(h->V, h->hidden, h->r, h->B, h->max_N, h->dtype, N, C);
+  char* w = (char*)ws;
+  float* xh = (float*)(w + L.xh);
+  void* lat = w + L.lat;
+  xp_status st = cuda_status(xp_launch_hidden(h, h_full, N, xh, (float*)(w + L.hmean),
+                                              (float*)(w + L.hc), (float*)(w + L.hcg), stream));
+  if (st != XP_OK) return st;
+  if (C == 0) {
+    st = cuda_status(xp_launch_init_argmax(h, base, sn, sb, anchor, N, blk, nullptr,
+                                           (unsigned long long*)(w + L.in_packed),
+                                           (unsigned*)(w + L.in_ticket), stream));
+    for (int k = 0; k < K && st == XP_OK; ++k) {
+      st = xp_latent_pass(h, blk, am1, xh, N, lat, stream);
+      if (st == XP_OK) st = readout_impl(h, lat, base, sn, sb, N, blk, nullptr, ws, stream);
+    }
+    return st;
+  }
+  int64_t* cand = (int64_t*)(w + L.cand);
+  void* base_c = w + L.base_c;
+  void* w2c = w + L.w2c;
+  st = cuda_status(
+      xp_launch_topc_gather(h, base, sn, sb, N, C, cand, base_c, w2c, blk, anchor, stream));
+  for (int k = 0; k < K && st == XP_OK; ++k) {
+    st = xp_latent_pass(h, blk, am1, xh, N, lat, stream);
+    if (st == XP_OK)
+      st = cuda_status(
+          xp_launch_topc_readout(h, lat, base_c, cand, w2c, N, C, blk, nullptr, stream));
+  }
+  return st;
+}
+
+xp_status xp_get_error(const xp_head* h, cudaStream_t stream) {
+  if (!h) return XP_ENOTPREPARED;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return XP_ECUDA;
+  uint32_t word = 0;
+  if (cudaMemcpy(&word, h->err, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return XP_ECUDA;
+  if (cudaMemset(h->err, 0, sizeof(word)) != cudaSuccess) return XP_ECUDA;
+  if (word & XP_ERR_TIMEOUT) return XP_ETIMEOUT;
+  if (word & XP_ERR_BADTOKEN) return XP_EBADTOKEN;
+  return XP_OK;
+}
+
+const char* xp_readout_kernel_name(const xp_head* h) {
+  if (!h) return "";
+  return h->readout_tc ? "readout_tc_kernel" : "readout_simt_kernel";
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+xp_encode_tiled_fn xp_get_encode_tiled() {
+  static xp_encode_tiled_fn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (xp_encode_tiled_fn)p;
+  }
+  return fn;
+}
+
+static void decide_paths(xp_head* h) {
+  h->readout_tc = 0;
+  h->latent_mma = 0;
+  int major = 0, minor = 0;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, h->device);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, h->device);
+  const bool blackwell = major == 10 && minor == 3;
+  if (!blackwell || h->dtype != XP_BF16) return;
+  // tcgen05 readout: K = r tiled by 64-wide (128-byte) swizzled chunks, at most 4
+  // of them resident; draft rows of one block never straddle a 128-row tile
+  if (h->r % 64 == 0 && h->r <= 256 && h->B - 1 <= 128 && xp_get_encode_tiled()) {
+    CUtensorMap tm;
+    const cuuint64_t dims[2] = {(cuuint64_t)h->r, (cuuint64_t)h->V};
+    const cuuint64_t strides[1] = {(cuuint64_t)h->r * 2};
+    const cuuint32_t box[2] = {64, 256};
+    const cuuint32_t es[2] = {1, 1};
+    if (xp_get_encode_tiled()(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, h->w2, dims, strides, box,
+                              es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS) {
+      h->tm_w2 = tm;
+      h->readout_tc = 1;
+    }
+  }
+  (void)h->latent_mma;
+}

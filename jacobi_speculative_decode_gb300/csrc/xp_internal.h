@@ -1,0 +1,80 @@
+// Internal declarations shared by the host API and the kernel translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "xp.h"
+
+// Host-side head: shapes, the prepared device copies, device facts.
+struct xp_head {
+  int V, hidden, r, H, B, max_N;
+  xp_dtype dtype;
+  int device, num_sms;
+  char* prep;            // caller-owned device memory holding everything below
+  size_t prep_bytes;
+  uint32_t* err;         // device error word (XP_ERR_* bits)
+  void *w1, *down_h, *down_g, *w_hc, *w_lat, *mix, *w_gate, *w_up, *w_down, *w2;
+  int readout_tc;        // tcgen05 readout usable for this head's shapes
+  int latent_mma;        // cluster tensor-core latent usable for this head's shapes
+  CUtensorMap tm_w2;     // W2 [V, r] tiled map for the tcgen05 readout
+};
+
+// device error word bits
+enum : uint32_t { XP_ERR_BADTOKEN = 1u, XP_ERR_TIMEOUT = 2u };
+
+// Workspace layout.  Regions that must stay zero between calls come first and
+// are sized by the head's max_N so that the layout never moves with N.
+struct xp_ws_layout {
+  size_t ro_packed, ro_ticket;        // readout argmax partials, per-row-tile tickets
+  size_t in_packed, in_ticket;        // init argmax partials, per-row tickets
+  size_t zero_end;                    // [0, zero_end) must be zero between calls
+  size_t xh, lat, hmean, hc, hcg;     // pass data
+  size_t cand, base_c, w2c;           // top-C tail (sized by the call's N and C)
+  size_t total;
+};
+xp_ws_layout xp_layout(int V, int hidden, int r, int B, int max_N, xp_dtype dt, int N, int C);
+
+static inline size_t xp_elem(xp_dtype d) { return d == XP_BF16 ? 2 : 4; }
+
+// ---- launchers (return cudaGetLastError() after launching) -----------------
+cudaError_t xp_launch_fold(const void* raw, void* mix, int r, int B, xp_dtype dt, cudaStream_t s);
+
+cudaError_t xp_launch_hidden(const xp_head* h, const void* h_full, int N, float* xh,
+                             float* hmean, float* hc, float* hcg, cudaStream_t s);
+
+cudaError_t xp_launch_init_argmax(const xp_head* h, const void* base, int64_t sn, int64_t sb,
+                                  const int64_t* anchor, int N, int64_t* blk, float* win,
+                                  unsigned long long* packed, unsigned* ticket, cudaStream_t s);
+
+cudaError_t xp_launch_latent_simt(const xp_head* h, const int64_t* blk, const int64_t* am1,
+                                  const float* xh, int N, void* lat, cudaStream_t s);
+cudaError_t xp_launch_latent_mma(const xp_head* h, const int64_t* blk, const int64_t* am1,
+                                 const float* xh, int N, void* lat, cudaStream_t s);
+
+cudaError_t xp_launch_readout_simt(const xp_head* h, const void* lat, const void* base,
+                                   int64_t sn, int64_t sb, int N, int64_t* blk, float* win,
+                                   unsigned long long* packed, unsigned* ticket, cudaStream_t s);
+// returns cudaErrorNotSupported when the call's base addressing cannot be tiled by TMA
+cudaError_t xp_launch_readout_tc(const xp_head* h, const void* lat, const void* base,
+                                 int64_t sn, int64_t sb, int N, int64_t* blk, float* win,
+                                 unsigned long long* packed, unsigned* ticket, cudaStream_t s);
+bool xp_readout_tc_call_ok(const xp_head* h, const void* lat, const void* base, int64_t sn,
+                           int64_t sb, int N);
+
+cudaError_t xp_launch_topc_gather(const xp_head* h, const void* base, int64_t sn, int64_t sb,
+                                  int N, int C, int64_t* cand, void* base_c, void* w2c,
+                                  int64_t* blk, const int64_t* anchor, cudaStream_t s);
+cudaError_t xp_launch_topc_readout(const xp_head* h, const void* lat, const void* base_c,
+                                   const int64_t* cand, const void* w2c, int N, int C,
+                                   int64_t* blk, float* win, cudaStream_t s);
+
+// tensor-map encoder fetched from the driver at run time (no -lcuda link)
+typedef CUresult (*xp_encode_tiled_fn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                       const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                       const cuuint32_t*, CUtensorMapInterleave,
+                                       CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                       CUtensorMapFloatOOBfill);
+xp_encode_tiled_fn xp_get_encode_tiled();

@@ -252,3 +252,9 @@ def random_lat(wl: Workload, seed: int, scale: float = 1.0) -> np.ndarray:
     """Synthetic latents [N, B-1, r] ~ N(0, scale^2) in storage form, for stage-only tests."""
     rng = np.random.default_rng(seed)
     return _normal(rng, (wl.N, wl.B - 1, wl.r), scale, wl.dtype)
+
+
+def random_xh(wl: Workload, seed: int) -> np.ndarray:
+    """Synthetic pass-invariant hidden projections [N, B, r] ~ N(0, 1), float32."""
+    rng = np.random.default_rng(seed)
+    return rng.standard_normal((wl.N, wl.B, wl.r), dtype=np.float32)
