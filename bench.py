@@ -1,0 +1,398 @@
+"""Benchmark: full-vocabulary Jacobi refinement on the batched-decode workload.
+
+One step = one ``xp_jacobi_refine`` call over a batch of N=32 draft blocks of
+B=16 slots, V=151936, bf16: the hidden cache, the init argmax and K=15 passes
+of latent + tensor-core readout/argmax.  ``value`` = Jacobi passes per second
+over the whole job (all ranks), inputs resident in HBM.  ``e2e`` = the same
+metric through the same C-ABI call with the step's inputs copied in from
+pinned host memory and blk copied back, every step.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+Multi-GPU (torchrun, one rank per GPU): every rank refines its own batch
+(weak scaling, no collective on the data path); timing is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+WORKLOAD = "batched-decode"
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "readout_tc_batched_decode.json")
+READOUT_SRC = os.path.join(ROOT, "jacobi_speculative_decode_gb300", "csrc", "k_readout_tc.cu")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-breakdown", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def src_hash(path):
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def committed_traffic(launch_rows):
+    """DRAM bytes per readout launch from the committed ncu summary, if the kernel is unchanged."""
+    try:
+        with open(PROFILE_TRAFFIC) as f:
+            p = json.load(f)
+        if p.get("source_sha256_16") != src_hash(READOUT_SRC) or p.get("rows") != launch_rows:
+            return None
+        return float(p["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+class Clocks:
+    """nvidia-smi sampled every 200 ms during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None:
+            return None
+        try:
+            rows = [ln.split(",") for ln in open(self.path).read().strip().splitlines() if ln.strip()]
+        except Exception:
+            return None
+        sm = [float(r[1]) for r in rows if len(r) >= 9 and r[1].strip().replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if len(r) >= 9 and r[2].strip().replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            if len(r) < 9:
+                continue
+            for name, val in zip(names, r[5:9]):
+                if val.strip().lower() in ("active", "1"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# native arm
+# ---------------------------------------------------------------------------
+
+def run_native(args, rank, world, local):
+    import torch
+    from jacobi_speculative_decode_gb300 import inputs as I
+    from jacobi_speculative_decode_gb300 import xp
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    wl = I.workload(args.workload)
+    d = I.make_inputs(wl)
+    head, _ = xp.head_from_inputs(d, wl)
+    base = xp.to_device(d["base"], wl.dtype)
+    h = xp.to_device(d["h_full"], wl.dtype)
+    anchor = torch.from_numpy(d["anchor"]).cuda()
+    am1 = torch.from_numpy(d["am1"]).cuda()
+    blk = torch.empty(wl.N, wl.B, dtype=torch.int64, device=dev)
+    ws = head.workspace(wl.N, wl.topc)
+    sn, sb = (wl.B - 1) * wl.V, wl.V
+    stream = torch.cuda.current_stream()
+
+    def step():
+        xp.xp_jacobi_refine(head.handle, base, sn, sb, h, anchor, am1, wl.N, wl.K, wl.topc, blk, ws)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        step()
+    status = xp.xp_get_error(head.handle)
+    if status != xp.XP_OK:
+        raise RuntimeError(f"device error after warm-up: {xp.status_str(status)}")
+
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with Clocks(local) as clk:
+        barrier()
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        barrier()
+    ms = e0.elapsed_time(e1)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    status = xp.xp_get_error(head.handle)
+    if status != xp.XP_OK:
+        raise RuntimeError(f"device error in the timed region: {xp.status_str(status)}")
+
+    passes = wl.K * args.steps * world
+    value = passes / (ms / 1e3)
+    launches_per_step = 5 + 1 + 2 * wl.K if wl.topc == 0 else 5 + 2 + 2 * wl.K
+    out = {
+        "metric": "Jacobi passes/s at N=32,B=16,V=151936 bf16; % of HBM roofline",
+        "value": round(value, 2), "unit": "passes/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded generator; random-init head weights)",
+        "config": {"workload": wl.name, "N": wl.N, "B": wl.B, "V": wl.V, "r": wl.r,
+                   "hidden": wl.hidden, "H": wl.H, "K": wl.K, "topc": wl.topc,
+                   "parallelism": f"blocks sharded, {world} independent replica(s)",
+                   "l2": "inputs larger than L2: base 146 MB + w2 78 MB streamed every pass"},
+        "rows_per_s": round(value * wl.rows, 1),
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk.summary(),
+    }
+
+    # --- per-kernel breakdown: the same pass issued stage by stage, events per kernel
+    if not args.no_breakdown:
+        out.update(breakdown(wl, head, base, sn, sb, h, anchor, am1, ws, stream, rank))
+
+    # --- end to end through the C ABI with host buffers
+    if not args.no_e2e:
+        out["e2e"] = e2e(wl, head, d, ws, args, stream, world)
+
+    if rank == 0 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(wl, d, budget_s=12.0)
+    head.close()
+    return out
+
+
+def breakdown(wl, head, base, sn, sb, h, anchor, am1, ws, stream, rank):
+    import torch
+    from jacobi_speculative_decode_gb300 import xp
+    rows = wl.rows
+    xh = torch.empty(wl.N, wl.B, wl.r, dtype=torch.float32, device="cuda")
+    lat = torch.empty(wl.N, wl.B - 1, wl.r, dtype=xp.torch_dtype(wl.dtype), device="cuda")
+    blk = torch.empty(wl.N, wl.B, dtype=torch.int64, device="cuda")
+    xp.xp_hidden_cache(head.handle, h, wl.N, xh, ws)
+    xp.xp_init_argmax(head.handle, base, sn, sb, anchor, wl.N, blk, None, ws)
+    n = max(3 * wl.K, 30)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+    for it in range(3):                       # warm
+        xp.xp_latent_pass(head.handle, blk, am1, xh, wl.N, lat)
+        xp.xp_readout_argmax(head.handle, lat, base, sn, sb, wl.N, blk, None, ws)
+    torch.cuda.synchronize()
+    for it in range(n):
+        ev[it][0].record(stream)
+        xp.xp_latent_pass(head.handle, blk, am1, xh, wl.N, lat)
+        ev[it][1].record(stream)
+        xp.xp_readout_argmax(head.handle, lat, base, sn, sb, wl.N, blk, None, ws)
+        ev[it][2].record(stream)
+    torch.cuda.synchronize()
+    lat_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    ro_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    # algorithmic bytes of one readout launch: w2 + base rows + latents in + blk out
+    es = 2 if wl.dtype == "bf16" else 4
+    ro_bytes = wl.V * wl.r * es + rows * wl.V * es + rows * wl.r * es + rows * 8
+    hbm, kind = peaks()
+    achieved = ro_bytes / (ro_ms / 1e3) / 1e9
+    traffic = committed_traffic(rows)
+    return {
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm,
+                     "unit": "GB/s", "frac": round(achieved / hbm, 4),
+                     "traffic": traffic, "kernel": xp.xp_readout_kernel_name(head.handle),
+                     "algorithmic_bytes_per_launch": ro_bytes,
+                     "peak_kind": f"{kind} (copy bandwidth, burst)"},
+        "kernel_us": {"readout_argmax": round(ro_ms * 1e3, 2), "latent": round(lat_ms * 1e3, 2)},
+        "latent_share_of_pass": round(lat_ms / (lat_ms + ro_ms), 4),
+    }
+
+
+def e2e(wl, head, d, ws, args, stream, world):
+    import torch
+    from jacobi_speculative_decode_gb300 import xp
+    pin = lambda a: xp.to_device(a, wl.dtype, device="cpu").pin_memory()
+    base_h = pin(d["base"])
+    h_h = pin(d["h_full"])
+    anc_h = torch.from_numpy(d["anchor"]).pin_memory()
+    am1_h = torch.from_numpy(d["am1"]).pin_memory()
+    blk_h = torch.empty(wl.N, wl.B, dtype=torch.int64).pin_memory()
+    base = torch.empty_like(base_h, device="cuda")
+    h = torch.empty_like(h_h, device="cuda")
+    anchor = torch.empty_like(anc_h, device="cuda")
+    am1 = torch.empty_like(am1_h, device="cuda")
+    blk = torch.empty(wl.N, wl.B, dtype=torch.int64, device="cuda")
+    sn, sb = (wl.B - 1) * wl.V, wl.V
+
+    def step():
+        base.copy_(base_h, non_blocking=True)
+        h.copy_(h_h, non_blocking=True)
+        anchor.copy_(anc_h, non_blocking=True)
+        am1.copy_(am1_h, non_blocking=True)
+        xp.xp_jacobi_refine(head.handle, base, sn, sb, h, anchor, am1, wl.N, wl.K, wl.topc, blk, ws)
+        blk_h.copy_(blk, non_blocking=True)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    steps = max(3, args.steps // 2)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    h2d = sum(t.numel() * t.element_size() for t in (base_h, h_h, anc_h, am1_h))
+    d2h = blk_h.numel() * blk_h.element_size()
+    return {"value": round(wl.K * steps * world / (ms / 1e3), 2), "unit": "passes/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": round(ms / steps, 4)}
+
+
+# ---------------------------------------------------------------------------
+# the fp64 CPU oracle as the baseline / reference arm
+# ---------------------------------------------------------------------------
+
+def cpu_baseline(wl, d, budget_s=12.0):
+    """Time the oracle as it stands on this host: hidden cache + init once, then full
+    passes over the whole batch until the budget is used; scaled to one step of K passes."""
+    from oracle import xp_oracle as O
+    p = O.params_from_inputs(d, wl.dtype)
+    base = O.decode(d["base"], wl.dtype)
+    hf = O.decode(d["h_full"], wl.dtype)
+    t0 = time.perf_counter()
+    xh = O.xh_from_cache(O.hidden_cache(hf, p.down_h, p.down_g), p.in_proj)
+    blk = O.init_blk(base, d["anchor"])
+    t_fixed = time.perf_counter() - t0
+    n = 0
+    t1 = time.perf_counter()
+    while True:
+        blk = O.full_pass(blk, d["am1"], xh, base, p)[0]
+        n += 1
+        if time.perf_counter() - t1 > budget_s or n >= wl.K:
+            break
+    t_pass = (time.perf_counter() - t1) / n
+    step_s = t_fixed + wl.K * t_pass
+    return {"value": round(wl.K / step_s, 4), "unit": "passes/s", "cores": os.cpu_count(),
+            "kind": "oracle",
+            "sample": f"hidden cache + init + {n} of {wl.K} full-vocabulary fp64 passes on the "
+                      f"whole {wl.N}-block batch, scaled to one {wl.K}-pass step"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    from jacobi_speculative_decode_gb300 import inputs as I
+    wl = I.workload(args.workload)
+    d = I.make_inputs(wl)
+    # every step is a bounded sample: one hidden cache + init + one pass, scaled to K passes
+    from oracle import xp_oracle as O
+    p = O.params_from_inputs(d, wl.dtype)
+    base = O.decode(d["base"], wl.dtype)
+    hf = O.decode(d["h_full"], wl.dtype)
+
+    def one_step():
+        t0 = time.perf_counter()
+        xh = O.xh_from_cache(O.hidden_cache(hf, p.down_h, p.down_g), p.in_proj)
+        blk = O.init_blk(base, d["anchor"])
+        tf = time.perf_counter() - t0
+        t1 = time.perf_counter()
+        O.full_pass(blk, d["am1"], xh, base, p)
+        return tf + wl.K * (time.perf_counter() - t1)
+
+    for _ in range(args.warmup):
+        one_step()
+    total = sum(one_step() for _ in range(args.steps))
+    value = wl.K * args.steps / total
+    return {"impl": "reference",
+            "metric": "Jacobi passes/s at N=32,B=16,V=151936 bf16; % of HBM roofline",
+            "value": round(value, 4), "unit": "passes/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(total / args.steps * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded generator; random-init head weights)",
+            "config": {"workload": wl.name, "N": wl.N, "B": wl.B, "V": wl.V, "r": wl.r,
+                       "hidden": wl.hidden, "H": wl.H, "K": wl.K, "topc": wl.topc},
+            "cpu_baseline": {"value": round(value, 4), "unit": "passes/s",
+                             "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": "per step: hidden cache + init + one fp64 full-vocabulary "
+                                       f"pass over the whole batch, scaled to {wl.K} passes"},
+            "e2e": {"value": round(value, 4), "unit": "passes/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        out = run_reference(args, rank, world)
+    else:
+        out = run_native(args, rank, world, local)
+    if rank == 0 and out is not None:
+        print(json.dumps(out), flush=True)
+    if world > 1 and args.impl == "native":
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

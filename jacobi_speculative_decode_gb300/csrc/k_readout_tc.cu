@@ -1,10 +1,343 @@
-// tcgen05 readout (placeholder until the tensor-core kernel lands).
-#include "xp_internal.h"
+// Tensor-core readout + argmax (sm_103a): blk[n, 1+b] = argmax_v base[n,b,v] + lat[n,b].w2[v]
+// (xpress kernels page, fused_add_argmax_to_blk with the w2 matmul of refine_bias fused in).
+//
+// One CTA owns a tile of up to 128 draft rows (whole blocks only) and a
+// contiguous range of 256-wide vocabulary tiles.  Per vocabulary tile:
+//   TMA   w2[v-tile, k-chunk]  (256 x 64 bf16, 128B-swizzled)  -> 2-stage smem ring
+//   TMA   base[rows, v-tile]   (two 64-wide boxes per half tile) -> 3-stage smem ring
+//   MMA   tcgen05 M=128 (rows) x N=256 (vocab) x K=r, fp32 accumulators in TMEM,
+//         double-buffered (2 x 256 columns)
+//   epilogue: each thread owns one row (one TMEM lane), adds base, keeps a
+//         running (max, lowest id) -- the logits never leave the SM.
+// The latent tile stays resident in smem for the whole kernel.  Per-row winners
+// of all CTAs of a row tile merge through a packed atomicMax; the CTA that
+// arrives last publishes into blk and resets the partials.
+//
+// Warp roles (224 threads): warp 0 base producer, warp 1 MMA issuer (+ TMEM
+// owner), warp 2 w2 producer, warps 3..6 epilogue (TMEM lane groups 3,0,1,2).
+#include <algorithm>
 
-bool xp_readout_tc_call_ok(const xp_head*, const void*, const void*, int64_t, int64_t, int) {
-  return false;
+#include "sm100_ptx.cuh"
+#include "xp_device.cuh"
+
+using namespace xpd;
+
+namespace {
+
+constexpr int BM = 128;           // rows per MMA (TMEM lanes)
+constexpr int BN = 256;           // vocabulary ids per tile (MMA N)
+constexpr int BK = 64;            // k per swizzled chunk (128 bytes of bf16)
+constexpr int W2_STAGES = 2;      // k-chunks of w2 in flight
+constexpr int BASE_STAGES = 3;    // half-tiles (128 ids) of base in flight
+constexpr int A_CHUNK_BYTES = BM * BK * 2;          // 16 KB
+constexpr int W2_STAGE_BYTES = BN * BK * 2;         // 32 KB
+constexpr int BASE_BOX_SLOT = 128 * 64 * 2;         // 16 KB slot per 64-wide box
+constexpr int BASE_STAGE_BYTES = 2 * BASE_BOX_SLOT; // 32 KB per half tile
+constexpr int NUM_THREADS = 224;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t IDESC = ptx::idesc_bf16_f32(BM, BN);
+
+struct Bars {
+  uint64_t a_full;
+  uint64_t w_full[W2_STAGES], w_empty[W2_STAGES];
+  uint64_t c_full[BASE_STAGES], c_empty[BASE_STAGES];
+  uint64_t t_full[2], t_empty[2];
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  int abort;
+  int last;
+};
+
+__device__ __forceinline__ float bf16lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
+
+template <int KCH>
+__global__ void __launch_bounds__(NUM_THREADS, 1) readout_tc_kernel(
+    const __grid_constant__ CUtensorMap tm_lat, const __grid_constant__ CUtensorMap tm_w2,
+    const __grid_constant__ CUtensorMap tm_base, int rows, int Bm1, int B, int V, int rpt, int bpt,
+    int n_rt, int n_seg, int nvt, int64_t* __restrict__ blk, float* __restrict__ win,
+    unsigned long long* __restrict__ packed, unsigned* __restrict__ ticket, uint32_t* err) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = ptx::smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  uint8_t* sA = smem;                                    // KCH x 16 KB
+  uint8_t* sW = sA + KCH * A_CHUNK_BYTES;                // W2_STAGES x 32 KB
+  uint8_t* sC = sW + W2_STAGES * W2_STAGE_BYTES;         // BASE_STAGES x 32 KB
+  Bars* bars = reinterpret_cast<Bars*>(sC + BASE_STAGES * BASE_STAGE_BYTES);
+  volatile int* abort = &bars->abort;
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int tile = blockIdx.x % n_rt, seg = blockIdx.x / n_rt;
+  const int vt0 = (int)((int64_t)seg * nvt / n_seg), vt1 = (int)((int64_t)(seg + 1) * nvt / n_seg);
+  const int row0 = tile * rpt;
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(ptx::smem_u32(&bars->a_full), 1);
+    for (int s = 0; s < W2_STAGES; ++s) {
+      ptx::mbar_init(ptx::smem_u32(&bars->w_full[s]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bars->w_empty[s]), 1);
+    }
+    for (int s = 0; s < BASE_STAGES; ++s) {
+      ptx::mbar_init(ptx::smem_u32(&bars->c_full[s]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bars->c_empty[s]), 4);
+    }
+    for (int s = 0; s < 2; ++s) {
+      ptx::mbar_init(ptx::smem_u32(&bars->t_full[s]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bars->t_empty[s]), 4);
+    }
+    ptx::mbar_init(ptx::smem_u32(&bars->mma_done), 1);
+    bars->abort = 0;
+    ptx::fence_barrier_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_u32(&bars->tmem_base), TMEM_COLS);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp == 0) {
+    // ---------------- base producer ----------------
+    if (lane == 0) {
+      ptx::prefetch_tmap(&tm_base);
+      const uint64_t pol = ptx::policy_evict_first();
+      const uint32_t box_bytes = 64u * (uint32_t)Bm1 * (uint32_t)bpt * 2u;
+      uint32_t issued[BASE_STAGES] = {};
+      int ci = 0;
+      bool ok = true;
+      for (int vt = vt0; vt < vt1 && ok; ++vt) {
+        for (int h = 0; h < 2 && ok; ++h, ++ci) {
+          const int s = ci % BASE_STAGES;
+          ok = ptx::mbar_wait(ptx::smem_u32(&bars->c_empty[s]), ((ci / BASE_STAGES) & 1) ^ 1,
+                              abort, err);
+          if (!ok) break;
+          const uint32_t full = ptx::smem_u32(&bars->c_full[s]);
+          ptx::mbar_arrive_expect_tx(full, 2 * box_bytes);
+          for (int q = 0; q < 2; ++q)
+            ptx::tma_load_3d(ptx::smem_u32(sC + s * BASE_STAGE_BYTES + q * BASE_BOX_SLOT),
+                             &tm_base, full, vt * BN + h * 128 + q * 64, 0, tile * bpt, pol);
+          ++issued[s];
+        }
+      }
+      // nothing may land in smem after the CTA is gone: wait for each stage's last load
+      for (int s = 0; s < BASE_STAGES; ++s)
+        if (issued[s]) {
+          volatile int no_abort = 0;
+          ptx::mbar_wait(ptx::smem_u32(&bars->c_full[s]), (issued[s] - 1) & 1, &no_abort, err);
+        }
+    }
+  } else if (warp == 2) {
+    // ---------------- latent + w2 producer ----------------
+    if (lane == 0) {
+      ptx::prefetch_tmap(&tm_lat);
+      ptx::prefetch_tmap(&tm_w2);
+      const uint64_t pol_keep = ptx::policy_evict_last();
+      const uint32_t a_full = ptx::smem_u32(&bars->a_full);
+      ptx::mbar_arrive_expect_tx(a_full, KCH * A_CHUNK_BYTES);
+      for (int kc = 0; kc < KCH; ++kc)
+        ptx::tma_load_2d(ptx::smem_u32(sA + kc * A_CHUNK_BYTES), &tm_lat, a_full, kc * BK, row0,
+                         pol_keep);
+      uint32_t issued[W2_STAGES] = {};
+      int wi = 0;
+      bool ok = true;
+      for (int vt = vt0; vt < vt1 && ok; ++vt) {
+        for (int kc = 0; kc < KCH; ++kc, ++wi) {
+          const int s = wi % W2_STAGES;
+          ok = ptx::mbar_wait(ptx::smem_u32(&bars->w_empty[s]), ((wi / W2_STAGES) & 1) ^ 1, abort,
+                              err);
+          if (!ok) break;
+          const uint32_t full = ptx::smem_u32(&bars->w_full[s]);
+          ptx::mbar_arrive_expect_tx(full, W2_STAGE_BYTES);
+          ptx::tma_load_2d(ptx::smem_u32(sW + s * W2_STAGE_BYTES), &tm_w2, full, kc * BK, vt * BN,
+                           pol_keep);
+          ++issued[s];
+        }
+      }
+      volatile int no_abort = 0;
+      ptx::mbar_wait(a_full, 0, &no_abort, err);
+      for (int s = 0; s < W2_STAGES; ++s)
+        if (issued[s])
+          ptx::mbar_wait(ptx::smem_u32(&bars->w_full[s]), (issued[s] - 1) & 1, &no_abort, err);
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      bool ok = ptx::mbar_wait(ptx::smem_u32(&bars->a_full), 0, abort, err);
+      ptx::tc_fence_after();
+      int wi = 0, ti = 0;
+      for (int vt = vt0; vt < vt1 && ok; ++vt, ++ti) {
+        const int buf = ti & 1;
+        ok = ptx::mbar_wait(ptx::smem_u32(&bars->t_empty[buf]), ((ti >> 1) & 1) ^ 1, abort, err);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        const uint32_t d = tmem + (uint32_t)(buf * BN);
+        for (int kc = 0; kc < KCH && ok; ++kc, ++wi) {
+          const int s = wi % W2_STAGES;
+          ok = ptx::mbar_wait(ptx::smem_u32(&bars->w_full[s]), (wi / W2_STAGES) & 1, abort, err);
+          if (!ok) break;
+          ptx::tc_fence_after();
+          const uint32_t a0 = ptx::smem_u32(sA + kc * A_CHUNK_BYTES);
+          const uint32_t b0 = ptx::smem_u32(sW + s * W2_STAGE_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)
+            ptx::mma_bf16(d, ptx::sw128_desc(a0 + kk * 32), ptx::sw128_desc(b0 + kk * 32), IDESC,
+                          (kc | kk) != 0);
+          ptx::mma_commit(ptx::smem_u32(&bars->w_empty[s]));
+        }
+        if (ok) ptx::mma_commit(ptx::smem_u32(&bars->t_full[buf]));
+      }
+      // every MMA this thread issued has finished before TMEM can be released
+      ptx::mma_commit(ptx::smem_u32(&bars->mma_done));
+      volatile int no_abort = 0;
+      ptx::mbar_wait(ptx::smem_u32(&bars->mma_done), 0, &no_abort, err);
+    }
+  } else {
+    // ---------------- epilogue: one row per thread ----------------
+    const int g = warp & 3;                  // TMEM lane group this warp may access
+    const int i = g * 32 + lane;             // row within the tile
+    const uint32_t trow = tmem + ((uint32_t)(g * 32) << 16);
+    float best = -INFINITY;
+    int bi = 0x7FFFFFFF;
+    int ti = 0, ci = 0;
+    bool ok = true;
+    for (int vt = vt0; vt < vt1 && ok; ++vt, ++ti) {
+      const int buf = ti & 1;
+      ok = ptx::mbar_wait(ptx::smem_u32(&bars->t_full[buf]), (ti >> 1) & 1, abort, err);
+      ok = __all_sync(0xFFFFFFFFu, ok);      // warp-uniform: tcgen05.ld is .sync.aligned
+      if (!ok) break;
+      ptx::tc_fence_after();
+      const int vbase = vt * BN;
+      for (int h = 0; h < 2 && ok; ++h, ++ci) {
+        const int s = ci % BASE_STAGES;
+        ok = ptx::mbar_wait(ptx::smem_u32(&bars->c_full[s]), (ci / BASE_STAGES) & 1, abort, err);
+        ok = __all_sync(0xFFFFFFFFu, ok);
+        if (!ok) break;
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const uint8_t* rowp = sC + s * BASE_STAGE_BYTES + q * BASE_BOX_SLOT + i * 128;
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc) {
+            const int col = h * 128 + q * 64 + cc * 32;
+            uint32_t acc[32];
+            ptx::tmem_ld32(trow + (uint32_t)(buf * BN + col), acc);
+            ptx::tmem_wait_ld();
+            const int vlim = V - (vbase + col);      // ids at or past V are padding
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch) {
+              const int lc = cc * 4 + ch;            // logical 16-byte chunk in the 128-byte row
+              const uint4 bv = *reinterpret_cast<const uint4*>(rowp + ((lc ^ (i & 7)) << 4));
+              const uint32_t w4[4] = {bv.x, bv.y, bv.z, bv.w};
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                const int idx = ch * 8 + e;
+                const float bval = (e & 1) ? bf16hi(w4[e >> 1]) : bf16lo(w4[e >> 1]);
+                const float sc = __uint_as_float(acc[idx]) + bval;
+                if (sc > best && idx < vlim) { best = sc; bi = vbase + col + idx; }
+              }
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->c_empty[s]));
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0 && ok) ptx::mbar_arrive(ptx::smem_u32(&bars->t_empty[buf]));
+    }
+    const int grow = row0 + i;
+    if (ok && !*abort && i < rpt && grow < rows && bi != 0x7FFFFFFF)
+      atomicMax(packed + grow, pack_best(best, (uint32_t)bi));
+  }
+
+  // ---------------- publish: the last CTA of this row tile writes blk ----------------
+  const bool last = arrive_last(ticket + tile, (unsigned)n_seg, &bars->last);
+  if (last && threadIdx.x < BM) {
+    const int grow = row0 + threadIdx.x;
+    if (threadIdx.x < rpt && grow < rows) {
+      const unsigned long long pk = atomicExch(packed + grow, 0ull);
+      const int n = grow / Bm1, b = grow % Bm1;
+      blk[(int64_t)n * B + 1 + b] = (int64_t)packed_idx(pk);
+      if (win) win[grow] = packed_val(pk);
+    }
+    if (threadIdx.x == 0) ticket[tile] = 0u;
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, TMEM_COLS);
+  }
 }
-cudaError_t xp_launch_readout_tc(const xp_head*, const void*, const void*, int64_t, int64_t, int,
-                                 int64_t*, float*, unsigned long long*, unsigned*, cudaStream_t) {
+
+constexpr size_t smem_bytes(int kch) {
+  return 1024 + (size_t)kch * A_CHUNK_BYTES + W2_STAGES * W2_STAGE_BYTES +
+         BASE_STAGES * BASE_STAGE_BYTES + sizeof(Bars);
+}
+
+bool encode(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* dims,
+            const cuuint64_t* strides, const cuuint32_t* box) {
+  xp_encode_tiled_fn fn = xp_get_encode_tiled();
+  if (!fn) return false;
+  const cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(ptr), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int KCH>
+cudaError_t launch(const xp_head* h, const CUtensorMap& tl, const CUtensorMap& tb, int N,
+                   int64_t* blk, float* win, unsigned long long* packed, unsigned* ticket,
+                   cudaStream_t s) {
+  const int Bm1 = h->B - 1, rows = N * Bm1;
+  const int bpt = BM / Bm1, rpt = bpt * Bm1;
+  const int n_rt = (N + bpt - 1) / bpt;
+  const int nvt = (h->V + BN - 1) / BN;
+  int n_seg = std::max(1, h->num_sms / n_rt);
+  n_seg = std::min(n_seg, nvt);
+  const size_t smem = smem_bytes(KCH);
+  cudaError_t e = cudaFuncSetAttribute(readout_tc_kernel<KCH>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  readout_tc_kernel<KCH><<<n_rt * n_seg, NUM_THREADS, smem, s>>>(
+      tl, h->tm_w2, tb, rows, Bm1, h->B, h->V, rpt, bpt, n_rt, n_seg, nvt, blk, win, packed,
+      ticket, h->err);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool xp_readout_tc_call_ok(const xp_head* h, const void* lat, const void* base, int64_t sn,
+                           int64_t sb, int N) {
+  return h->readout_tc && N > 0 && (uintptr_t)lat % 16 == 0 && (uintptr_t)base % 16 == 0 &&
+         sn % 8 == 0 && sb % 8 == 0 && sb >= h->V && sn >= (int64_t)(h->B - 1) * sb;
+}
+
+cudaError_t xp_launch_readout_tc(const xp_head* h, const void* lat, const void* base, int64_t sn,
+                                 int64_t sb, int N, int64_t* blk, float* win,
+                                 unsigned long long* packed, unsigned* ticket, cudaStream_t s) {
+  if (!xp_readout_tc_call_ok(h, lat, base, sn, sb, N)) return cudaErrorNotSupported;
+  const int Bm1 = h->B - 1;
+  const int bpt = BM / Bm1;
+  CUtensorMap tl, tb;
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)h->r, (cuuint64_t)N * Bm1};
+    const cuuint64_t strides[1] = {(cuuint64_t)h->r * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)BM};
+    if (!encode(&tl, lat, 2, dims, strides, box)) return cudaErrorNotSupported;
+  }
+  {
+    const cuuint64_t dims[3] = {(cuuint64_t)h->V, (cuuint64_t)Bm1, (cuuint64_t)N};
+    const cuuint64_t strides[2] = {(cuuint64_t)sb * 2, (cuuint64_t)sn * 2};
+    const cuuint32_t box[3] = {64, (cuuint32_t)Bm1, (cuuint32_t)bpt};
+    if (!encode(&tb, base, 3, dims, strides, box)) return cudaErrorNotSupported;
+  }
+  switch (h->r / BK) {
+    case 1: return launch<1>(h, tl, tb, N, blk, win, packed, ticket, s);
+    case 2: return launch<2>(h, tl, tb, N, blk, win, packed, ticket, s);
+    case 3: return launch<3>(h, tl, tb, N, blk, win, packed, ticket, s);
+    case 4: return launch<4>(h, tl, tb, N, blk, win, packed, ticket, s);
+  }
   return cudaErrorNotSupported;
 }

@@ -226,9 +226,11 @@ static xp_status readout_impl(const xp_head* h, const void* lat, const void* bas
   char* w = (char*)ws;
   auto* packed = (unsigned long long*)(w + L.ro_packed);
   auto* ticket = (unsigned*)(w + L.ro_ticket);
-  if (h->readout_tc && xp_readout_tc_call_ok(h, lat, base, sn, sb, N))
-    return cuda_status(
-        xp_launch_readout_tc(h, lat, base, sn, sb, N, blk, win, packed, ticket, stream));
+  if (h->readout_tc && xp_readout_tc_call_ok(h, lat, base, sn, sb, N)) {
+    const cudaError_t e =
+        xp_launch_readout_tc(h, lat, base, sn, sb, N, blk, win, packed, ticket, stream);
+    if (e != cudaErrorNotSupported) return cuda_status(e);
+  }
   return cuda_status(
       xp_launch_readout_simt(h, lat, base, sn, sb, N, blk, win, packed, ticket, stream));
 }
@@ -363,6 +365,7 @@ static void decide_paths(xp_head* h) {
   cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, h->device);
   const bool blackwell = major == 10 && minor == 3;
   if (!blackwell || h->dtype != XP_BF16) return;
+  h->latent_mma = xp_latent_mma_ok(h->r, h->H, h->B, h->dtype) ? 1 : 0;
   // tcgen05 readout: K = r tiled by 64-wide (128-byte) swizzled chunks, at most 4
   // of them resident; draft rows of one block never straddle a 128-row tile
   if (h->r % 64 == 0 && h->r <= 256 && h->B - 1 <= 128 && xp_get_encode_tiled()) {
@@ -379,5 +382,4 @@ static void decide_paths(xp_head* h) {
       h->readout_tc = 1;
     }
   }
-  (void)h->latent_mma;
 }

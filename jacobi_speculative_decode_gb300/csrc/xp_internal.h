@@ -51,6 +51,7 @@ cudaError_t xp_launch_init_argmax(const xp_head* h, const void* base, int64_t sn
 
 cudaError_t xp_launch_latent_simt(const xp_head* h, const int64_t* blk, const int64_t* am1,
                                   const float* xh, int N, void* lat, cudaStream_t s);
+bool xp_latent_mma_ok(int r, int H, int B, xp_dtype dt);
 cudaError_t xp_launch_latent_mma(const xp_head* h, const int64_t* blk, const int64_t* am1,
                                  const float* xh, int N, void* lat, cudaStream_t s);
 

@@ -21,8 +21,9 @@ WORKLOADS = [
     I.workload("batched-decode", V=5000, hidden=512, N=20, K=4),
     I.workload("single-request", V=4104, hidden=256, B=5, N=40, K=4, base_kind="peaks_half_ties"),
     I.workload("batched-decode", V=4099, hidden=128, r=64, H=128, N=6, K=3),
+    I.workload("batched-decode", V=2056, hidden=96, r=96, H=80, B=6, N=7, K=3),
 ]
-IDS = ["tiny-fp32", "bf16-V5000-B16", "bf16-B5", "bf16-oddV-r64"]
+IDS = ["tiny-fp32", "bf16-V5000-B16", "bf16-B5", "bf16-oddV-r64", "bf16-r96-plain"]
 
 
 @pytest.fixture(scope="module", params=list(range(len(WORKLOADS))), ids=IDS)
