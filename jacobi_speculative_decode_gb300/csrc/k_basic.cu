@@ -1,5 +1,4 @@
-// Plain CUDA kernels of the pass: the mixer fold, the hidden cache, the
-// streaming init argmax, and SIMT versions of the latent stage and of the
+// Plain CUDA kernels of the pass: the mixer fold, the streaming init argmax, and SIMT versions of the latent stage and of the
 // readout (used for fp32 heads and for shapes the tensor-core kernels do not
 // tile).  All accumulate in fp32.
 #include <math.h>
@@ -39,113 +38,6 @@ cudaError_t xp_launch_fold(const void* raw, void* mix, int r, int B, xp_dtype dt
 }
 
 // ---------------------------------------------------------------------------
-// hidden cache (qwen3_xpress page, hidden_cache + the xh hoist):
-//   hmean[n]          = mean_b h[n, b]
-//   hc[n*B+b, 0:r]    = down_h h[n, b]
-//   hc[n*B+b, r:2r]   = down_g hmean[n]          (broadcast over b)
-//   xh[n*B+b]         = w_hc hc[n*B+b]            (w_hc = in_proj[:, :2r])
-// ---------------------------------------------------------------------------
-template <typename T>
-__global__ void block_mean_kernel(const T* __restrict__ h, float* __restrict__ g, int N, int B,
-                                  int hid) {
-  const int n = blockIdx.y;
-  for (int k = blockIdx.x * blockDim.x + threadIdx.x; k < hid; k += gridDim.x * blockDim.x) {
-    float s = 0.f;
-    for (int b = 0; b < B; ++b) s += to_f(h[((size_t)n * B + b) * hid + k]);
-    g[(size_t)n * hid + k] = s / (float)B;
-  }
-}
-
-// C[m, n] = sum_k A[m, k] B[n, k]   (both operands K-contiguous), fp32 out
-template <typename TA, typename TB>
-__global__ void __launch_bounds__(256) gemm_nt_kernel(const TA* __restrict__ A, int lda,
-                                                      const TB* __restrict__ Bm, int ldb,
-                                                      float* __restrict__ C, int ldc, int M,
-                                                      int Nn, int K) {
-  __shared__ float As[16][64 + 1];
-  __shared__ float Bs[16][64 + 1];
-  const int tid = threadIdx.x, tx = tid % 16, ty = tid / 16;
-  const int m0 = blockIdx.y * 64, n0 = blockIdx.x * 64;
-  float acc[4][4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-  for (int k0 = 0; k0 < K; k0 += 16) {
-    for (int i = tid; i < 64 * 16; i += 256) {
-      const int mm = i / 16, kk = i % 16, gk = k0 + kk;
-      const int gm = m0 + mm, gn = n0 + mm;
-      As[kk][mm] = (gm < M && gk < K) ? to_f(A[(size_t)gm * lda + gk]) : 0.f;
-      Bs[kk][mm] = (gn < Nn && gk < K) ? to_f(Bm[(size_t)gn * ldb + gk]) : 0.f;
-    }
-    __syncthreads();
-#pragma unroll
-    for (int kk = 0; kk < 16; ++kk) {
-      float a[4], b[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) a[i] = As[kk][ty + 16 * i];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) b[j] = Bs[kk][tx + 16 * j];
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
-    }
-    __syncthreads();
-  }
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int m = m0 + ty + 16 * i;
-    if (m >= M) continue;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int n = n0 + tx + 16 * j;
-      if (n < Nn) C[(size_t)m * ldc + n] = acc[i][j];
-    }
-  }
-}
-
-__global__ void bcast_rows_kernel(const float* __restrict__ src, float* __restrict__ dst, int N,
-                                  int B, int r) {
-  // dst[(n*B+b)*2r + r + c] = src[n*r + c]
-  const size_t total = (size_t)N * B * r;
-  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total;
-       i += (size_t)gridDim.x * blockDim.x) {
-    const int c = (int)(i % r);
-    const size_t nb = i / r;
-    const int n = (int)(nb / B);
-    dst[nb * 2 * r + r + c] = src[(size_t)n * r + c];
-  }
-}
-
-template <typename TA, typename TB>
-static void gemm_nt(const TA* A, int lda, const TB* Bm, int ldb, float* C, int ldc, int M, int Nn,
-                    int K, cudaStream_t s) {
-  dim3 grid((Nn + 63) / 64, (M + 63) / 64);
-  gemm_nt_kernel<TA, TB><<<grid, 256, 0, s>>>(A, lda, Bm, ldb, C, ldc, M, Nn, K);
-}
-
-template <typename T>
-static cudaError_t hidden_impl(const xp_head* h, const T* hf, int N, float* xh, float* hmean,
-                               float* hc, float* hcg, cudaStream_t s) {
-  const int B = h->B, hid = h->hidden, r = h->r;
-  dim3 mg((hid + 255) / 256, N);
-  block_mean_kernel<T><<<mg, 256, 0, s>>>(hf, hmean, N, B, hid);
-  gemm_nt<T, T>(hf, hid, (const T*)h->down_h, hid, hc, 2 * r, N * B, r, hid, s);
-  gemm_nt<float, T>(hmean, hid, (const T*)h->down_g, hid, hcg, r, N, r, hid, s);
-  const size_t tot = (size_t)N * B * r;
-  bcast_rows_kernel<<<(unsigned)((tot + 255) / 256), 256, 0, s>>>(hcg, hc, N, B, r);
-  gemm_nt<float, T>(hc, 2 * r, (const T*)h->w_hc, 2 * r, xh, r, N * B, r, 2 * r, s);
-  return cudaGetLastError();
-}
-
-cudaError_t xp_launch_hidden(const xp_head* h, const void* h_full, int N, float* xh, float* hmean,
-                             float* hc, float* hcg, cudaStream_t s) {
-  if (h->dtype == XP_BF16) return hidden_impl(h, (const bf16*)h_full, N, xh, hmean, hc, hcg, s);
-  return hidden_impl(h, (const float*)h_full, N, xh, hmean, hc, hcg, s);
-}
-
-// ---------------------------------------------------------------------------
 // init argmax: blk[n,0] = anchor[n]; blk[n,1+b] = argmax_v base[n,b,v]
 // (qwen3_xpress page, jacobi_refine_greedy before the passes).  Grid
 // (splits, rows); each CTA reduces one vocabulary chunk of one row, the last
@@ -170,13 +62,25 @@ __global__ void __launch_bounds__(256) init_argmax_kernel(
   if (VEC) {
     constexpr int E = 16 / sizeof(T);
     const int nvec = (v1 - v0) / E;
-    for (int i = threadIdx.x; i < nvec; i += blockDim.x) {
-      const uint4 q = __ldg(reinterpret_cast<const uint4*>(p + v0 + i * E));
-      const T* e = reinterpret_cast<const T*>(&q);
+    constexpr int U = 4;                         // 16-byte loads in flight per thread
+    for (int i0 = threadIdx.x; i0 < nvec; i0 += U * blockDim.x) {
+      uint4 q[U];
 #pragma unroll
-      for (int k = 0; k < E; ++k) {
-        const float x = to_f(e[k]);
-        if (x > best) { best = x; bi = v0 + i * E + k; }
+      for (int u = 0; u < U; ++u) {
+        const int i = i0 + u * blockDim.x;
+        q[u] = i < nvec ? __ldcs(reinterpret_cast<const uint4*>(p + v0 + i * E))
+                        : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int i = i0 + u * blockDim.x;
+        if (i >= nvec) break;
+        const T* e = reinterpret_cast<const T*>(&q[u]);
+#pragma unroll
+        for (int k = 0; k < E; ++k) {
+          const float x = to_f(e[k]);
+          if (x > best) { best = x; bi = v0 + i * E + k; }
+        }
       }
     }
     vtail = v0 + nvec * E;

@@ -45,7 +45,7 @@ __host__ __device__ inline Smem smem_plan(int r, int H, int B) {
   s.wg = take(HS * s.pk_r * 2);
   s.wu = take(HS * s.pk_r * 2);
   s.wd = take(CS * s.pk_h * 2);
-  s.mix = take(CS * B * B * 2);
+  s.mix = take(B * B * (CS + 1) * 4);     // fp32, [out slot][in slot][channel]
   s.ufull = take(MT * s.pk_r * 2);
   // the embeddings (phase 1) and the gathered activations (phase 3) share one region
   s.afull = take(std::max(MT * s.pk_h * 2, MT * s.pk_r * 2));
@@ -60,6 +60,10 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
                "l"(src)
                : "memory");
+}
+__device__ __forceinline__ void pdl_wait_all() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.wait_all;" ::: "memory");
@@ -97,6 +101,33 @@ __device__ __forceinline__ void tile_mma(float (&acc)[4], const bf16* A, int lda
   }
 }
 
+// Copy the column slices [p*W, (p+1)*W) of buf (MT rows, pitch elements) from every
+// other CTA p of the cluster into this CTA's buf; four 16-byte loads in flight per thread.
+__device__ __forceinline__ void gather_peers(cg::cluster_group& cluster, bf16* buf, int pitch,
+                                             int W, int q, int tid) {
+  const int chunks = W / 8;
+  const int total = (CL - 1) * MT * chunks;
+  for (int i0 = tid; i0 < total; i0 += 4 * THREADS) {
+    uint4 v[4];
+    int off[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + u * THREADS;
+      off[u] = -1;
+      if (i < total) {
+        const int pp = i / (MT * chunks), rem = i % (MT * chunks);
+        const int p = pp + (pp >= q);
+        const int m = rem / chunks, cc = rem % chunks;
+        off[u] = m * pitch + p * W + cc * 8;
+        v[u] = *reinterpret_cast<const uint4*>(cluster.map_shared_rank(buf, p) + off[u]);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (off[u] >= 0) *reinterpret_cast<uint4*>(buf + off[u]) = v[u];
+  }
+}
+
 __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1) latent_mma_kernel(
     const int64_t* __restrict__ blk, const int64_t* __restrict__ am1, const float* __restrict__ xh,
     const bf16* __restrict__ w1, const bf16* __restrict__ wlat, const bf16* __restrict__ mix,
@@ -112,7 +143,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1) latent_
   bf16* sWg = (bf16*)(sm + P.wg);
   bf16* sWu = (bf16*)(sm + P.wu);
   bf16* sWd = (bf16*)(sm + P.wd);
-  bf16* sMix = (bf16*)(sm + P.mix);
+  float* sMix = (float*)(sm + P.mix);
   bf16* sU = (bf16*)(sm + P.ufull);
   bf16* sA = (bf16*)(sm + P.afull);        // embeddings first, activations later
   float* sX = (float*)(sm + P.xs);
@@ -136,12 +167,15 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1) latent_
     stage(sWg, P.pk_r, wg + (int64_t)q * HS * r, HS, r);
     stage(sWu, P.pk_r, wu + (int64_t)q * HS * r, HS, r);
     stage(sWd, P.pk_h, wd + (int64_t)q * CS * H, CS, H);
-    const int mchunks = CS * B * B / 8;
-    for (int i = tid; i < mchunks; i += THREADS)
-      cp_async16(sMix + i * 8, mix + (int64_t)q * CS * B * B + i * 8);
+  }
+  // mixer slice, transposed to [b][j][c] so that neighbouring channels hit neighbouring banks
+  for (int i = tid; i < CS * B * B; i += THREADS) {
+    const int c = i / (B * B), bj = i % (B * B);
+    sMix[bj * (CS + 1) + c] = __bfloat162float(mix[(int64_t)q * CS * B * B + i]);
   }
 
-  // ---- token ids and embeddings ----
+  // ---- token ids and embeddings (written by the previous kernel) ----
+  pdl_wait_all();
   for (int m = tid; m < MT; m += THREADS) {
     int64_t t = 0;
     if (m < rows) {
@@ -163,6 +197,8 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1) latent_
   }
   cp_async_wait_all();
   __syncthreads();
+
+  pdl_trigger();
 
   // ---- phase 1: x (own channels) = xh + emb . w_lat^T ----
   for (int it = warp; it < (MT / 16) * (CS / 8); it += THREADS / 32) {
@@ -187,8 +223,8 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1) latent_
     float u = 0.f;
     if (m < rows) {
       const int bl = m / B, b = m % B;
-      const bf16* mrow = sMix + (c * B + b) * B;
-      for (int j = 0; j < B; ++j) u = fmaf(__bfloat162float(mrow[j]), sX[(bl * B + j) * (CS + 1) + c], u);
+      const float* mcol = sMix + b * B * (CS + 1) + c;
+      for (int j = 0; j < B; ++j) u = fmaf(mcol[j * (CS + 1)], sX[(bl * B + j) * (CS + 1) + c], u);
     }
     sUs[m * (CS + 1) + c] = u;
     sU[m * P.pk_r + q * CS + c] = __float2bfloat16_rn(u);
@@ -196,17 +232,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1) latent_
   cluster.sync();
 
   // ---- gather the other CTAs' u slices ----
-  {
-    const int chunks = CS / 8;
-    for (int i = tid; i < (CL - 1) * MT * chunks; i += THREADS) {
-      const int pp = i / (MT * chunks), rem = i % (MT * chunks);
-      const int p = pp + (pp >= q);
-      const int m = rem / chunks, cc = rem % chunks;
-      const int off = m * P.pk_r + p * CS + cc * 8;
-      const bf16* src = cluster.map_shared_rank(sU, p) + off;
-      *reinterpret_cast<uint4*>(sU + off) = *reinterpret_cast<const uint4*>(src);
-    }
-  }
+  gather_peers(cluster, sU, P.pk_r, CS, q, tid);
   __syncthreads();
 
   // ---- phase 2: SwiGLU on own hidden units: a = silu(u w_gate^T) * (u w_up^T) ----
@@ -226,17 +252,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1) latent_
   cluster.sync();
 
   // ---- gather the other CTAs' activation slices ----
-  {
-    const int chunks = HS / 8;
-    for (int i = tid; i < (CL - 1) * MT * chunks; i += THREADS) {
-      const int pp = i / (MT * chunks), rem = i % (MT * chunks);
-      const int p = pp + (pp >= q);
-      const int m = rem / chunks, cc = rem % chunks;
-      const int off = m * P.pk_h + p * HS + cc * 8;
-      const bf16* src = cluster.map_shared_rank(sA, p) + off;
-      *reinterpret_cast<uint4*>(sA + off) = *reinterpret_cast<const uint4*>(src);
-    }
-  }
+  gather_peers(cluster, sA, P.pk_h, HS, q, tid);
   __syncthreads();
 
   // ---- phase 3: lat (own channels) = u + a . w_down^T, slots 1..B-1 ----
@@ -275,9 +291,9 @@ cudaError_t xp_launch_latent_mma(const xp_head* h, const int64_t* blk, const int
   cudaError_t e = cudaFuncSetAttribute(latent_mma_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, P.total);
   if (e != cudaSuccess) return e;
-  latent_mma_kernel<<<clusters * CL, THREADS, P.total, s>>>(
-      blk, am1, xh, (const bf16*)h->w1, (const bf16*)h->w_lat, (const bf16*)h->mix,
-      (const bf16*)h->w_gate, (const bf16*)h->w_up, (const bf16*)h->w_down, (bf16*)lat, N, h->B,
-      h->r, h->H, h->V, h->err);
-  return cudaGetLastError();
+  e = xp_launch_pdl(latent_mma_kernel, dim3(clusters * CL), dim3(THREADS), (size_t)P.total, s, blk,
+                    am1, xh, (const bf16*)h->w1, (const bf16*)h->w_lat, (const bf16*)h->mix,
+                    (const bf16*)h->w_gate, (const bf16*)h->w_up, (const bf16*)h->w_down,
+                    (bf16*)lat, N, h->B, h->r, h->H, h->V, h->err);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }

@@ -3,8 +3,8 @@
 //
 // One CTA owns a tile of up to 128 draft rows (whole blocks only) and a
 // contiguous range of 256-wide vocabulary tiles.  Per vocabulary tile:
-//   TMA   w2[v-tile, k-chunk]  (256 x 64 bf16, 128B-swizzled)  -> 2-stage smem ring
-//   TMA   base[rows, v-tile]   (two 64-wide boxes per half tile) -> 3-stage smem ring
+//   TMA   w2[v-tile, k-chunk]  (256 x 64 bf16, 128B-swizzled)  -> 3-stage smem ring
+//   TMA   base[rows, 64 ids]   (one box per quarter tile)        -> 4-stage smem ring
 //   MMA   tcgen05 M=128 (rows) x N=256 (vocab) x K=r, fp32 accumulators in TMEM,
 //         double-buffered (2 x 256 columns)
 //   epilogue: each thread owns one row (one TMEM lane), adds base, keeps a
@@ -27,12 +27,11 @@ namespace {
 constexpr int BM = 128;           // rows per MMA (TMEM lanes)
 constexpr int BN = 256;           // vocabulary ids per tile (MMA N)
 constexpr int BK = 64;            // k per swizzled chunk (128 bytes of bf16)
-constexpr int W2_STAGES = 2;      // k-chunks of w2 in flight
-constexpr int BASE_STAGES = 3;    // half-tiles (128 ids) of base in flight
+constexpr int W2_STAGES = 3;      // k-chunks of w2 in flight (w2 is 2/3 of each SM's stream)
+constexpr int BASE_STAGES = 4;    // quarter tiles (64 ids) of base in flight
 constexpr int A_CHUNK_BYTES = BM * BK * 2;          // 16 KB
 constexpr int W2_STAGE_BYTES = BN * BK * 2;         // 32 KB
-constexpr int BASE_BOX_SLOT = 128 * 64 * 2;         // 16 KB slot per 64-wide box
-constexpr int BASE_STAGE_BYTES = 2 * BASE_BOX_SLOT; // 32 KB per half tile
+constexpr int BASE_STAGE_BYTES = 128 * 64 * 2;      // 16 KB: one 64-wide box of <= 128 rows
 constexpr int NUM_THREADS = 224;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t IDESC = ptx::idesc_bf16_f32(BM, BN);
@@ -97,6 +96,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) readout_tc_kernel(
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
+  ptx::pdl_trigger();
 
   if (warp == 0) {
     // ---------------- base producer ----------------
@@ -108,16 +108,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) readout_tc_kernel(
       int ci = 0;
       bool ok = true;
       for (int vt = vt0; vt < vt1 && ok; ++vt) {
-        for (int h = 0; h < 2 && ok; ++h, ++ci) {
+        for (int qt = 0; qt < BN / 64 && ok; ++qt, ++ci) {
           const int s = ci % BASE_STAGES;
           ok = ptx::mbar_wait(ptx::smem_u32(&bars->c_empty[s]), ((ci / BASE_STAGES) & 1) ^ 1,
                               abort, err);
           if (!ok) break;
           const uint32_t full = ptx::smem_u32(&bars->c_full[s]);
-          ptx::mbar_arrive_expect_tx(full, 2 * box_bytes);
-          for (int q = 0; q < 2; ++q)
-            ptx::tma_load_3d(ptx::smem_u32(sC + s * BASE_STAGE_BYTES + q * BASE_BOX_SLOT),
-                             &tm_base, full, vt * BN + h * 128 + q * 64, 0, tile * bpt, pol);
+          ptx::mbar_arrive_expect_tx(full, box_bytes);
+          ptx::tma_load_3d(ptx::smem_u32(sC + s * BASE_STAGE_BYTES), &tm_base, full,
+                           vt * BN + qt * 64, 0, tile * bpt, pol);
           ++issued[s];
         }
       }
@@ -135,15 +134,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) readout_tc_kernel(
       ptx::prefetch_tmap(&tm_w2);
       const uint64_t pol_keep = ptx::policy_evict_last();
       const uint32_t a_full = ptx::smem_u32(&bars->a_full);
-      ptx::mbar_arrive_expect_tx(a_full, KCH * A_CHUNK_BYTES);
-      for (int kc = 0; kc < KCH; ++kc)
-        ptx::tma_load_2d(ptx::smem_u32(sA + kc * A_CHUNK_BYTES), &tm_lat, a_full, kc * BK, row0,
-                         pol_keep);
       uint32_t issued[W2_STAGES] = {};
       int wi = 0;
       bool ok = true;
+      bool have_a = false;
       for (int vt = vt0; vt < vt1 && ok; ++vt) {
         for (int kc = 0; kc < KCH; ++kc, ++wi) {
+          if (!have_a && wi == W2_STAGES) {
+            // w2 needs nothing from the previous kernel; the latents do
+            ptx::pdl_wait();
+            ptx::mbar_arrive_expect_tx(a_full, KCH * A_CHUNK_BYTES);
+            for (int k = 0; k < KCH; ++k)
+              ptx::tma_load_2d(ptx::smem_u32(sA + k * A_CHUNK_BYTES), &tm_lat, a_full, k * BK,
+                               row0, pol_keep);
+            have_a = true;
+          }
           const int s = wi % W2_STAGES;
           ok = ptx::mbar_wait(ptx::smem_u32(&bars->w_empty[s]), ((wi / W2_STAGES) & 1) ^ 1, abort,
                               err);
@@ -154,6 +159,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) readout_tc_kernel(
                            pol_keep);
           ++issued[s];
         }
+      }
+      if (!have_a) {
+        ptx::pdl_wait();
+        ptx::mbar_arrive_expect_tx(a_full, KCH * A_CHUNK_BYTES);
+        for (int k = 0; k < KCH; ++k)
+          ptx::tma_load_2d(ptx::smem_u32(sA + k * A_CHUNK_BYTES), &tm_lat, a_full, k * BK, row0,
+                           pol_keep);
       }
       volatile int no_abort = 0;
       ptx::mbar_wait(a_full, 0, &no_abort, err);
@@ -209,33 +221,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) readout_tc_kernel(
       if (!ok) break;
       ptx::tc_fence_after();
       const int vbase = vt * BN;
-      for (int h = 0; h < 2 && ok; ++h, ++ci) {
+      for (int qt = 0; qt < BN / 64 && ok; ++qt, ++ci) {
         const int s = ci % BASE_STAGES;
         ok = ptx::mbar_wait(ptx::smem_u32(&bars->c_full[s]), (ci / BASE_STAGES) & 1, abort, err);
         ok = __all_sync(0xFFFFFFFFu, ok);
         if (!ok) break;
+        const uint8_t* rowp = sC + s * BASE_STAGE_BYTES + i * 128;
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          const uint8_t* rowp = sC + s * BASE_STAGE_BYTES + q * BASE_BOX_SLOT + i * 128;
+        for (int cc = 0; cc < 2; ++cc) {
+          const int col = qt * 64 + cc * 32;
+          uint32_t acc[32];
+          ptx::tmem_ld32(trow + (uint32_t)(buf * BN + col), acc);
+          ptx::tmem_wait_ld();
+          const int vlim = V - (vbase + col);        // ids at or past V are padding
 #pragma unroll
-          for (int cc = 0; cc < 2; ++cc) {
-            const int col = h * 128 + q * 64 + cc * 32;
-            uint32_t acc[32];
-            ptx::tmem_ld32(trow + (uint32_t)(buf * BN + col), acc);
-            ptx::tmem_wait_ld();
-            const int vlim = V - (vbase + col);      // ids at or past V are padding
+          for (int ch = 0; ch < 4; ++ch) {
+            const int lc = cc * 4 + ch;              // logical 16-byte chunk in the 128-byte row
+            const uint4 bv = *reinterpret_cast<const uint4*>(rowp + ((lc ^ (i & 7)) << 4));
+            const uint32_t w4[4] = {bv.x, bv.y, bv.z, bv.w};
 #pragma unroll
-            for (int ch = 0; ch < 4; ++ch) {
-              const int lc = cc * 4 + ch;            // logical 16-byte chunk in the 128-byte row
-              const uint4 bv = *reinterpret_cast<const uint4*>(rowp + ((lc ^ (i & 7)) << 4));
-              const uint32_t w4[4] = {bv.x, bv.y, bv.z, bv.w};
-#pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                const int idx = ch * 8 + e;
-                const float bval = (e & 1) ? bf16hi(w4[e >> 1]) : bf16lo(w4[e >> 1]);
-                const float sc = __uint_as_float(acc[idx]) + bval;
-                if (sc > best && idx < vlim) { best = sc; bi = vbase + col + idx; }
-              }
+            for (int e = 0; e < 8; ++e) {
+              const int idx = ch * 8 + e;
+              const float bval = (e & 1) ? bf16hi(w4[e >> 1]) : bf16lo(w4[e >> 1]);
+              const float sc = __uint_as_float(acc[idx]) + bval;
+              if (sc > best && idx < vlim) { best = sc; bi = vbase + col + idx; }
             }
           }
         }
@@ -252,6 +261,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) readout_tc_kernel(
   }
 
   // ---------------- publish: the last CTA of this row tile writes blk ----------------
+  ptx::pdl_wait();            // blk may still be read by the kernel this one overlapped
   const bool last = arrive_last(ticket + tile, (unsigned)n_seg, &bars->last);
   if (last && threadIdx.x < BM) {
     const int grow = row0 + threadIdx.x;
@@ -300,10 +310,10 @@ cudaError_t launch(const xp_head* h, const CUtensorMap& tl, const CUtensorMap& t
   cudaError_t e = cudaFuncSetAttribute(readout_tc_kernel<KCH>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  readout_tc_kernel<KCH><<<n_rt * n_seg, NUM_THREADS, smem, s>>>(
-      tl, h->tm_w2, tb, rows, Bm1, h->B, h->V, rpt, bpt, n_rt, n_seg, nvt, blk, win, packed,
-      ticket, h->err);
-  return cudaGetLastError();
+  e = xp_launch_pdl(readout_tc_kernel<KCH>, dim3(n_rt * n_seg), dim3(NUM_THREADS), smem, s, tl,
+                    h->tm_w2, tb, rows, Bm1, h->B, h->V, rpt, bpt, n_rt, n_seg, nvt, blk, win,
+                    packed, ticket, h->err);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace

@@ -28,7 +28,7 @@ bool valid_weight_ptrs(const xp_weights* w) {
 }
 
 struct PrepLayout {
-  size_t err, w1, down_h, down_g, w_hc, w_lat, mix, w_gate, w_up, w_down, w2, total;
+  size_t err, w1, down_hg, w_hc, w_lat, mix, w_gate, w_up, w_down, w2, total;
 };
 
 PrepLayout prep_layout(const xp_weights* w) {
@@ -39,8 +39,7 @@ PrepLayout prep_layout(const xp_weights* w) {
   auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes); return at; };
   L.err = take(256);
   L.w1 = take(V * r * es);
-  L.down_h = take(r * hid * es);
-  L.down_g = take(r * hid * es);
+  L.down_hg = take(2 * r * hid * es);
   L.w_hc = take(r * 2 * r * es);
   L.w_lat = take(r * r * es);
   L.mix = take(r * B * B * es);
@@ -60,8 +59,8 @@ xp_status copy_weights(xp_head* h, const xp_weights* w, cudaStream_t s) {
     if (e == cudaSuccess) e = cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, s);
   };
   cp(h->w1, w->w1, V * r * es);
-  cp(h->down_h, w->down_h, r * hid * es);
-  cp(h->down_g, w->down_g, r * hid * es);
+  cp(h->down_hg, w->down_h, r * hid * es);
+  cp((char*)h->down_hg + r * hid * es, w->down_g, r * hid * es);
   // in_proj [r, 3r]: columns [0, 2r) act on the hidden cache, [2r, 3r) on the embedding
   if (e == cudaSuccess)
     e = cudaMemcpy2DAsync(h->w_hc, 2 * r * es, w->in_proj, 3 * r * es, 2 * r * es, r,
@@ -88,6 +87,7 @@ bool valid_base(const xp_head* h, const void* base, int64_t sn, int64_t sb) {
 // ---------------------------------------------------------------------------
 xp_ws_layout xp_layout(int V, int hidden, int r, int B, int max_N, xp_dtype dt, int N, int C) {
   (void)V;
+  (void)hidden;
   const size_t es = xp_elem(dt);
   const size_t rows_cap = (size_t)max_N * (B - 1);
   xp_ws_layout L;
@@ -100,9 +100,9 @@ xp_ws_layout xp_layout(int V, int hidden, int r, int B, int max_N, xp_dtype dt, 
   L.zero_end = o;
   L.xh = take((size_t)max_N * B * r * 4);
   L.lat = take(rows_cap * r * es);
-  L.hmean = take((size_t)max_N * hidden * 4);
+  L.part_rows = std::max(4096, max_N * B);
+  L.part = take((size_t)L.part_rows * 2 * r * 4);
   L.hc = take((size_t)max_N * B * 2 * r * 4);
-  L.hcg = take((size_t)max_N * r * 4);
   const size_t rows = (size_t)std::max(N, 0) * (B - 1);
   const size_t c = (size_t)std::max(C, 0);
   L.cand = take(rows * c * 8);
@@ -168,7 +168,7 @@ xp_status xp_head_create(const xp_weights* w, void* prep_dev, size_t prep_bytes,
   }
   char* p = h->prep;
   h->err = (uint32_t*)(p + L.err);
-  h->w1 = p + L.w1; h->down_h = p + L.down_h; h->down_g = p + L.down_g;
+  h->w1 = p + L.w1; h->down_hg = p + L.down_hg;
   h->w_hc = p + L.w_hc; h->w_lat = p + L.w_lat; h->mix = p + L.mix;
   h->w_gate = p + L.w_gate; h->w_up = p + L.w_up; h->w_down = p + L.w_down; h->w2 = p + L.w2;
   xp_status st = copy_weights(h, w, stream);
@@ -205,8 +205,8 @@ xp_status xp_hidden_cache(const xp_head* h, const void* h_full, int N, float* xh
   if (N == 0) return XP_OK;
   const xp_ws_layout L = xp_layout(h->V, h->hidden, h->r, h->B, h->max_N, h->dtype, N, 0);
   char* w = (char*)ws;
-  return cuda_status(xp_launch_hidden(h, h_full, N, xh, (float*)(w + L.hmean), (float*)(w + L.hc),
-                                      (float*)(w + L.hcg), stream));
+  return cuda_status(xp_launch_hidden(h, h_full, N, xh, (float*)(w + L.part), (float*)(w + L.hc),
+                                      L.part_rows, stream));
 }
 
 xp_status xp_latent_pass(const xp_head* h, const int64_t* blk, const int64_t* am1,
@@ -295,8 +295,8 @@ xp_status xp_jacobi_refine(const xp_head* h, const void* base, int64_t sn, int64
   char* w = (char*)ws;
   float* xh = (float*)(w + L.xh);
   void* lat = w + L.lat;
-  xp_status st = cuda_status(xp_launch_hidden(h, h_full, N, xh, (float*)(w + L.hmean),
-                                              (float*)(w + L.hc), (float*)(w + L.hcg), stream));
+  xp_status st = cuda_status(xp_launch_hidden(h, h_full, N, xh, (float*)(w + L.part),
+                                              (float*)(w + L.hc), L.part_rows, stream));
   if (st != XP_OK) return st;
   if (C == 0) {
     st = cuda_status(xp_launch_init_argmax(h, base, sn, sb, anchor, N, blk, nullptr,

@@ -16,7 +16,7 @@ struct xp_head {
   char* prep;            // caller-owned device memory holding everything below
   size_t prep_bytes;
   uint32_t* err;         // device error word (XP_ERR_* bits)
-  void *w1, *down_h, *down_g, *w_hc, *w_lat, *mix, *w_gate, *w_up, *w_down, *w2;
+  void *w1, *down_hg, *w_hc, *w_lat, *mix, *w_gate, *w_up, *w_down, *w2;  // down_hg = [down_h ; down_g]
   int readout_tc;        // tcgen05 readout usable for this head's shapes
   int latent_mma;        // cluster tensor-core latent usable for this head's shapes
   CUtensorMap tm_w2;     // W2 [V, r] tiled map for the tcgen05 readout
@@ -31,7 +31,8 @@ struct xp_ws_layout {
   size_t ro_packed, ro_ticket;        // readout argmax partials, per-row-tile tickets
   size_t in_packed, in_ticket;        // init argmax partials, per-row tickets
   size_t zero_end;                    // [0, zero_end) must be zero between calls
-  size_t xh, lat, hmean, hc, hcg;     // pass data
+  size_t xh, lat, part, hc;           // pass data and hidden-cache scratch
+  int part_rows;                      // rows of fp32 split-K partials the scratch holds
   size_t cand, base_c, w2c;           // top-C tail (sized by the call's N and C)
   size_t total;
 };
@@ -42,8 +43,8 @@ static inline size_t xp_elem(xp_dtype d) { return d == XP_BF16 ? 2 : 4; }
 // ---- launchers (return cudaGetLastError() after launching) -----------------
 cudaError_t xp_launch_fold(const void* raw, void* mix, int r, int B, xp_dtype dt, cudaStream_t s);
 
-cudaError_t xp_launch_hidden(const xp_head* h, const void* h_full, int N, float* xh,
-                             float* hmean, float* hc, float* hcg, cudaStream_t s);
+cudaError_t xp_launch_hidden(const xp_head* h, const void* h_full, int N, float* xh, float* part,
+                             float* hc, int part_rows, cudaStream_t s);
 
 cudaError_t xp_launch_init_argmax(const xp_head* h, const void* base, int64_t sn, int64_t sb,
                                   const int64_t* anchor, int N, int64_t* blk, float* win,
@@ -71,6 +72,25 @@ cudaError_t xp_launch_topc_gather(const xp_head* h, const void* base, int64_t sn
 cudaError_t xp_launch_topc_readout(const xp_head* h, const void* lat, const void* base_c,
                                    const int64_t* cand, const void* w2c, int N, int C,
                                    int64_t* blk, float* win, cudaStream_t s);
+
+// Launch with a programmatic dependency on the previous kernel in the stream:
+// the kernel's prologue may overlap that kernel's tail; the kernel itself must
+// call griddepcontrol.wait before it touches anything the predecessor writes.
+template <typename... KArgs, typename... Args>
+cudaError_t xp_launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
 
 // tensor-map encoder fetched from the driver at run time (no -lcuda link)
 typedef CUresult (*xp_encode_tiled_fn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
