@@ -13,8 +13,9 @@
 // of all CTAs of a row tile merge through a packed atomicMax; the CTA that
 // arrives last publishes into blk and resets the partials.
 //
-// Warp roles (224 threads): warp 0 base producer, warp 1 MMA issuer (+ TMEM
-// owner), warp 2 w2 producer, warps 3..6 epilogue (TMEM lane groups 3,0,1,2).
+// Warp roles (352 threads): warp 0 base producer, warp 1 MMA issuer (+ TMEM
+// owner), warp 2 w2 producer, warps 3..10 epilogue: warp w reads TMEM lane
+// group w % 4 and half (w - 3) / 4 of every 256-wide tile.
 #include <algorithm>
 
 #include "sm100_ptx.cuh"
@@ -32,7 +33,7 @@ constexpr int BASE_STAGES = 4;    // quarter tiles (64 ids) of base in flight
 constexpr int A_CHUNK_BYTES = BM * BK * 2;          // 16 KB
 constexpr int W2_STAGE_BYTES = BN * BK * 2;         // 32 KB
 constexpr int BASE_STAGE_BYTES = 128 * 64 * 2;      // 16 KB: one 64-wide box of <= 128 rows
-constexpr int NUM_THREADS = 224;
+constexpr int NUM_THREADS = 352;   // 3 producer/MMA warps + 8 epilogue warps
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t IDESC = ptx::idesc_bf16_f32(BM, BN);
 
@@ -78,11 +79,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) readout_tc_kernel(
     }
     for (int s = 0; s < BASE_STAGES; ++s) {
       ptx::mbar_init(ptx::smem_u32(&bars->c_full[s]), 1);
-      ptx::mbar_init(ptx::smem_u32(&bars->c_empty[s]), 4);
+      ptx::mbar_init(ptx::smem_u32(&bars->c_empty[s]), 4);   // the 4 warps of one half
     }
     for (int s = 0; s < 2; ++s) {
       ptx::mbar_init(ptx::smem_u32(&bars->t_full[s]), 1);
-      ptx::mbar_init(ptx::smem_u32(&bars->t_empty[s]), 4);
+      ptx::mbar_init(ptx::smem_u32(&bars->t_empty[s]), 8);   // all 8 epilogue warps
     }
     ptx::mbar_init(ptx::smem_u32(&bars->mma_done), 1);
     bars->abort = 0;
@@ -206,13 +207,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) readout_tc_kernel(
       ptx::mbar_wait(ptx::smem_u32(&bars->mma_done), 0, &no_abort, err);
     }
   } else {
-    // ---------------- epilogue: one row per thread ----------------
+    // ---------------- epilogue: one row per thread, half of each tile per warp ----------------
+    static_assert(BASE_STAGES == BN / 64, "one base stage per quarter tile");
     const int g = warp & 3;                  // TMEM lane group this warp may access
+    const int half = (warp - 3) >> 2;        // which 128 ids of every tile
     const int i = g * 32 + lane;             // row within the tile
     const uint32_t trow = tmem + ((uint32_t)(g * 32) << 16);
     float best = -INFINITY;
     int bi = 0x7FFFFFFF;
-    int ti = 0, ci = 0;
+    int ti = 0;
     bool ok = true;
     for (int vt = vt0; vt < vt1 && ok; ++vt, ++ti) {
       const int buf = ti & 1;
@@ -221,19 +224,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) readout_tc_kernel(
       if (!ok) break;
       ptx::tc_fence_after();
       const int vbase = vt * BN;
-      for (int qt = 0; qt < BN / 64 && ok; ++qt, ++ci) {
-        const int s = ci % BASE_STAGES;
-        ok = ptx::mbar_wait(ptx::smem_u32(&bars->c_full[s]), (ci / BASE_STAGES) & 1, abort, err);
+      for (int qq = 0; qq < 2 && ok; ++qq) {
+        const int qt = half * 2 + qq;        // quarter tile == base ring stage
+        ok = ptx::mbar_wait(ptx::smem_u32(&bars->c_full[qt]), ti & 1, abort, err);
         ok = __all_sync(0xFFFFFFFFu, ok);
         if (!ok) break;
-        const uint8_t* rowp = sC + s * BASE_STAGE_BYTES + i * 128;
+        const uint8_t* rowp = sC + qt * BASE_STAGE_BYTES + i * 128;
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
           const int col = qt * 64 + cc * 32;
           uint32_t acc[32];
           ptx::tmem_ld32(trow + (uint32_t)(buf * BN + col), acc);
           ptx::tmem_wait_ld();
-          const int vlim = V - (vbase + col);        // ids at or past V are padding
+          float sc[32];
 #pragma unroll
           for (int ch = 0; ch < 4; ++ch) {
             const int lc = cc * 4 + ch;              // logical 16-byte chunk in the 128-byte row
@@ -241,15 +244,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) readout_tc_kernel(
             const uint32_t w4[4] = {bv.x, bv.y, bv.z, bv.w};
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-              const int idx = ch * 8 + e;
               const float bval = (e & 1) ? bf16hi(w4[e >> 1]) : bf16lo(w4[e >> 1]);
-              const float sc = __uint_as_float(acc[idx]) + bval;
-              if (sc > best && idx < vlim) { best = sc; bi = vbase + col + idx; }
+              sc[ch * 8 + e] = __uint_as_float(acc[ch * 8 + e]) + bval;
             }
+          }
+          const int vlim = V - (vbase + col);        // ids at or past V are padding
+          if (vlim < 32) {                           // warp-uniform: only the last tile
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              if (e >= vlim) sc[e] = -INFINITY;
+          }
+          // chunk maximum first; the lowest index of it only when it beats the row's best
+          float m = sc[0];
+#pragma unroll
+          for (int e = 1; e < 32; ++e) m = fmaxf(m, sc[e]);
+          if (m > best) {
+            int first = 31;
+#pragma unroll
+            for (int e = 31; e >= 0; --e)
+              if (sc[e] == m) first = e;
+            best = m;
+            bi = vbase + col + first;
           }
         }
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->c_empty[s]));
+        if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->c_empty[qt]));
       }
       ptx::tc_fence_before();
       __syncwarp();

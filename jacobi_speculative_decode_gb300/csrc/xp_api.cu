@@ -28,7 +28,7 @@ bool valid_weight_ptrs(const xp_weights* w) {
 }
 
 struct PrepLayout {
-  size_t err, w1, down_hg, w_hc, w_lat, mix, w_gate, w_up, w_down, w2, total;
+  size_t err, w1, down_hg, w_hc, w_lat, mix, mixT, w_gate, w_up, w_down, w2, total;
 };
 
 PrepLayout prep_layout(const xp_weights* w) {
@@ -43,6 +43,7 @@ PrepLayout prep_layout(const xp_weights* w) {
   L.w_hc = take(r * 2 * r * es);
   L.w_lat = take(r * r * es);
   L.mix = take(r * B * B * es);
+  L.mixT = take(r * B * B * 4);
   L.w_gate = take(H * r * es);
   L.w_up = take(H * r * es);
   L.w_down = take(r * H * es);
@@ -69,6 +70,7 @@ xp_status copy_weights(xp_head* h, const xp_weights* w, cudaStream_t s) {
     e = cudaMemcpy2DAsync(h->w_lat, r * es, (const char*)w->in_proj + 2 * r * es, 3 * r * es,
                           r * es, r, cudaMemcpyDeviceToDevice, s);
   cp(h->mix, w->mix_L, r * B * B * es);
+  if (e == cudaSuccess) e = xp_launch_mix_transpose(h->mix, h->mixT, (int)r, (int)B, w->dtype, s);
   cp(h->w_gate, w->w_gate, H * r * es);
   cp(h->w_up, w->w_up, H * r * es);
   cp(h->w_down, w->w_down, r * H * es);
@@ -170,6 +172,7 @@ xp_status xp_head_create(const xp_weights* w, void* prep_dev, size_t prep_bytes,
   h->err = (uint32_t*)(p + L.err);
   h->w1 = p + L.w1; h->down_hg = p + L.down_hg;
   h->w_hc = p + L.w_hc; h->w_lat = p + L.w_lat; h->mix = p + L.mix;
+  h->mixT = (float*)(p + L.mixT);
   h->w_gate = p + L.w_gate; h->w_up = p + L.w_up; h->w_down = p + L.w_down; h->w2 = p + L.w2;
   xp_status st = copy_weights(h, w, stream);
   if (st == XP_OK) st = cuda_status(cudaMemsetAsync(h->err, 0, 256, stream));
