@@ -37,24 +37,25 @@ cudaError_t xp_launch_fold(const void* raw, void* mix, int r, int B, xp_dtype dt
   return cudaGetLastError();
 }
 
-// mixT[(b*B + j)*r + c] = mix[(c*B + b)*B + j], widened to fp32 (a prepared layout)
+// mixT[(b*B + j)*r + c] = mix[(c*B + b)*B + j]: the folded mixer with the channel
+// innermost (a prepared layout, like the pages' mix_kjc), same storage type
 template <typename T>
-__global__ void mix_transpose_kernel(const T* __restrict__ mix, float* __restrict__ mixT, int r,
+__global__ void mix_transpose_kernel(const T* __restrict__ mix, T* __restrict__ mixT, int r,
                                      int B) {
   const int total = r * B * B;
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
     const int c = i % r, bj = i / r;
-    mixT[i] = to_f(mix[(int64_t)c * B * B + bj]);
+    mixT[i] = mix[(int64_t)c * B * B + bj];
   }
 }
 
-cudaError_t xp_launch_mix_transpose(const void* mix, float* mixT, int r, int B, xp_dtype dt,
+cudaError_t xp_launch_mix_transpose(const void* mix, void* mixT, int r, int B, xp_dtype dt,
                                     cudaStream_t s) {
   const int grid = (r * B * B + 255) / 256;
   if (dt == XP_BF16)
-    mix_transpose_kernel<bf16><<<grid, 256, 0, s>>>((const bf16*)mix, mixT, r, B);
+    mix_transpose_kernel<bf16><<<grid, 256, 0, s>>>((const bf16*)mix, (bf16*)mixT, r, B);
   else
-    mix_transpose_kernel<float><<<grid, 256, 0, s>>>((const float*)mix, mixT, r, B);
+    mix_transpose_kernel<float><<<grid, 256, 0, s>>>((const float*)mix, (float*)mixT, r, B);
   return cudaGetLastError();
 }
 

@@ -8,16 +8,23 @@
 // The cluster splits the work by output features so each CTA holds only 1/8 of
 // the weights: CTA q owns channels [q*r/8, (q+1)*r/8) of the in_proj and
 // w_down products and hidden units [q*H/8, (q+1)*H/8) of the SwiGLU.  Its
-// weight slices are copied into shared memory once, before the kernel waits
-// on the previous pass, and stay there while the cluster walks over groups of
-// MT rows (whole blocks).  The full u and SwiGLU activations of a group are
-// exchanged through distributed shared memory.  Products use mma.sync
-// m16n8k16 (bf16 in, fp32 accumulate); the mixer, the K-split partial sums
-// (added in a fixed order) and the residual stay in fp32.
+// weight and mixer slices arrive by TMA once, before the kernel waits on the
+// previous pass, and stay in shared memory while the cluster walks over groups
+// of MT rows (whole blocks).  Per group the embeddings and the xh slice arrive
+// by cp.async; the full u and SwiGLU activations are exchanged through
+// distributed shared memory.  Products use mma.sync m16n8k16 (bf16 in, fp32
+// accumulate); the mixer, the K-split partial sums (added in a fixed order)
+// and the residual stay in fp32.
+//
+// Every bf16 matrix in shared memory uses the TMA 128-byte-swizzle layout in
+// 64-column chunks: element (row, k) of an R-row matrix lives at
+//   (k / 64) * R * 128 + row * 128 + ((((k % 64) / 8) ^ (row % 8)) * 16) + (k % 8) * 2
+// so ldmatrix row reads hit eight distinct bank groups without padding.
 #include <cooperative_groups.h>
 
 #include <algorithm>
 
+#include "sm100_ptx.cuh"
 #include "xp_device.cuh"
 
 namespace cg = cooperative_groups;
@@ -31,58 +38,65 @@ constexpr int THREADS = 256;   // 8 warps
 constexpr int NW = THREADS / 32;
 
 struct Plan {                  // shapes and byte offsets into dynamic shared memory
-  int MT, CS, HS, pk_r, pk_h;
+  int MT, CS, HS;
   int nt1, ks1;                // in_proj / w_down: n-tiles of the CTA's channels, K splits
-  int wlat, wg, wu, wd, ufull, afull, part, us, prev;
+  int wlat, wg, wu, wd, mix, ea, u, xh, part, us, prev, bar;
+  int mix_rows;                // B*B
   int total;
 };
 
-__host__ __device__ inline Plan make_plan(int MT, int r, int H) {
+__host__ __device__ inline Plan make_plan(int MT, int r, int H, int B) {
   Plan p;
   p.MT = MT;
   p.CS = r / CL;
   p.HS = H / CL;
-  p.pk_r = r + 8;              // padded pitches keep ldmatrix rows on distinct banks
-  p.pk_h = H + 8;
   p.nt1 = p.CS / 8;
-  // K splits: fill the warps, but keep every split a whole number of 16-wide k-steps
+  // K splits: fill the warps, keep every split a whole number of 16-wide k-steps
   p.ks1 = std::min(NW / p.nt1, std::min(r, H) / 16);
+  p.mix_rows = B * B;
+  const int mparts = (p.mix_rows + 255) / 256, mbox = std::min(p.mix_rows, 256);
   int o = 0;
-  auto take = [&](int bytes) { int at = o; o += (bytes + 127) / 128 * 128; return at; };
-  p.wlat = take(p.CS * p.pk_r * 2);
-  p.wg = take(p.HS * p.pk_r * 2);
-  p.wu = take(p.HS * p.pk_r * 2);
-  p.wd = take(p.CS * p.pk_h * 2);
-  p.ufull = take(MT * p.pk_r * 2);
-  // embeddings (phase 1) and gathered activations (phase 3) share one region
-  p.afull = take(std::max(MT * p.pk_h * 2, MT * p.pk_r * 2));
-  p.part = take(p.ks1 * MT * (p.CS + 1) * 4);   // K-split partial sums
-  p.us = take(MT * (p.CS + 1) * 4);             // x, then u (fp32)
-  p.prev = take(MT * 8);
+  // TMA / swizzled regions 1024-byte aligned, the rest 16-byte aligned
+  auto take = [&](int bytes, int align) {
+    o = (o + align - 1) / align * align;
+    const int at = o;
+    o += bytes;
+    return at;
+  };
+  p.wlat = take(p.CS * r * 2, 1024);
+  p.wg = take(p.HS * r * 2, 1024);
+  p.wu = take(p.HS * r * 2, 1024);
+  p.wd = take(p.CS * H * 2, 1024);
+  p.mix = take(mparts * mbox * p.CS * 2, 1024);
+  p.ea = take(MT * std::max(r, H) * 2, 1024);   // embeddings, later the activations
+  p.u = take(MT * r * 2, 1024);
+  p.xh = take(MT * p.CS * 4, 16);
+  p.part = take(p.ks1 * MT * (p.CS + 1) * 4, 16);
+  p.us = take(MT * (p.CS + 1) * 4, 16);
+  p.prev = take(MT * 8, 16);
+  p.bar = take(16, 16);
   p.total = o;
   return p;
 }
 
-__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
-                   (uint32_t)__cvta_generic_to_shared(dst)),
-               "l"(src)
-               : "memory");
+// byte offset of element (row, k) of an R-row swizzled matrix
+__device__ __forceinline__ int swz(int row, int k, int R) {
+  return ((k >> 6) * R + row) * 128 + ((((k & 63) >> 3) ^ (row & 7)) << 4) + ((k & 7) << 1);
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void pdl_trigger() {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-__device__ __forceinline__ void ldm_x4(uint32_t (&r)[4], const void* p) {
+__device__ __forceinline__ void ldm_x4(uint32_t (&r)[4], uint32_t addr) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"((uint32_t)__cvta_generic_to_shared(p)));
+               : "r"(addr));
 }
-__device__ __forceinline__ void ldm_x2(uint32_t (&r)[2], const void* p) {
+__device__ __forceinline__ void ldm_x2(uint32_t (&r)[2], uint32_t addr) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];"
                : "=r"(r[0]), "=r"(r[1])
-               : "r"((uint32_t)__cvta_generic_to_shared(p)));
+               : "r"(addr));
 }
 __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4],
                                          const uint32_t (&b)[2]) {
@@ -93,21 +107,22 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4],
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
 
-// acc[i] (16x8, rows 16i..) += A[rows, k0:k1] . Bt[n0:n0+8, k0:k1]^T for every m-tile i:
-// one B fragment per k-step feeds MTILES independent MMAs.
+// acc[i] += A[16i.., k0:k1] . B[n0..n0+8, k0:k1]^T for every m-tile i (A: MT rows, B: RB
+// rows, both swizzled).  One B fragment per k-step feeds MTILES independent MMAs.
 template <int MTILES>
-__device__ __forceinline__ void warp_gemm(float (&acc)[MTILES][4], const bf16* A, int lda,
-                                          const bf16* Bt, int ldb, int n0, int k0, int k1) {
+__device__ __forceinline__ void warp_gemm(float (&acc)[MTILES][4], uint32_t A, uint32_t Bm, int RB,
+                                          int n0, int k0, int k1) {
+  constexpr int MT = MTILES * 16;
   const int lane = threadIdx.x % 32;
-  const bf16* ap = A + (lane % 16) * lda + (lane / 16) * 8;
-  const bf16* bp = Bt + (n0 + (lane % 8)) * ldb + ((lane / 8) % 2) * 8;
+  const int ar = lane % 16, ak = (lane / 16) * 8;
+  const int br = n0 + (lane % 8), bk = ((lane / 8) % 2) * 8;
   for (int k = k0; k < k1; k += 16) {
     uint32_t b[2];
-    ldm_x2(b, bp + k);
+    ldm_x2(b, Bm + swz(br, k + bk, RB));
 #pragma unroll
     for (int i = 0; i < MTILES; ++i) {
       uint32_t a[4];
-      ldm_x4(a, ap + i * 16 * lda + k);
+      ldm_x4(a, A + swz(i * 16 + ar, k + ak, MT));
       mma16816(acc[i], a, b);
     }
   }
@@ -116,103 +131,120 @@ __device__ __forceinline__ void warp_gemm(float (&acc)[MTILES][4], const bf16* A
 // Same for two B operands (gate and up) sharing every A fragment.
 template <int MTILES>
 __device__ __forceinline__ void warp_gemm_pair(float (&acc0)[MTILES][4], float (&acc1)[MTILES][4],
-                                               const bf16* A, int lda, const bf16* B0,
-                                               const bf16* B1, int ldb, int n0, int K) {
+                                               uint32_t A, uint32_t B0, uint32_t B1, int RB,
+                                               int n0, int K) {
+  constexpr int MT = MTILES * 16;
   const int lane = threadIdx.x % 32;
-  const bf16* ap = A + (lane % 16) * lda + (lane / 16) * 8;
-  const int boff = (n0 + (lane % 8)) * ldb + ((lane / 8) % 2) * 8;
+  const int ar = lane % 16, ak = (lane / 16) * 8;
+  const int br = n0 + (lane % 8), bk = ((lane / 8) % 2) * 8;
   for (int k = 0; k < K; k += 16) {
     uint32_t b0[2], b1[2];
-    ldm_x2(b0, B0 + boff + k);
-    ldm_x2(b1, B1 + boff + k);
+    const int bo = swz(br, k + bk, RB);
+    ldm_x2(b0, B0 + bo);
+    ldm_x2(b1, B1 + bo);
 #pragma unroll
     for (int i = 0; i < MTILES; ++i) {
       uint32_t a[4];
-      ldm_x4(a, ap + i * 16 * lda + k);
+      ldm_x4(a, A + swz(i * 16 + ar, k + ak, MT));
       mma16816(acc0[i], a, b0);
       mma16816(acc1[i], a, b1);
     }
   }
 }
 
-// Copy columns [p*W, (p+1)*W) of buf (MT rows x pitch) from every other CTA p of the
-// cluster into this CTA's buf; four 16-byte loads in flight per thread.
-__device__ __forceinline__ void gather_peers(cg::cluster_group& cluster, bf16* buf, int MT,
-                                             int pitch, int W, int q) {
-  const int chunks = W / 8;
+// Copy the columns [p*W, (p+1)*W) of a swizzled MT-row matrix from every other CTA p of
+// the cluster into this CTA's copy (same offsets everywhere); all loads issued first.
+template <int MTILES, int PER>
+__device__ __forceinline__ void gather_peers(cg::cluster_group& cluster, uint8_t* buf, int W,
+                                             int q) {
+  constexpr int MT = MTILES * 16;
+  const int chunks = W / 8;                       // 16-byte chunks per row and peer
   const int total = (CL - 1) * MT * chunks;
-  for (int i0 = threadIdx.x; i0 < total; i0 += 4 * THREADS) {
-    uint4 v[4];
-    int off[4];
+  for (int i0 = threadIdx.x; i0 < total; i0 += PER * THREADS) {
+    uint4 v[PER];
+    int off[PER];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < PER; ++u) {
       const int i = i0 + u * THREADS;
       off[u] = -1;
       if (i < total) {
         const int pp = i / (MT * chunks), rem = i % (MT * chunks);
         const int p = pp + (pp >= q);
         const int m = rem / chunks, cc = rem % chunks;
-        off[u] = m * pitch + p * W + cc * 8;
+        off[u] = swz(m, p * W + cc * 8, MT);
         v[u] = *reinterpret_cast<const uint4*>(cluster.map_shared_rank(buf, p) + off[u]);
       }
     }
 #pragma unroll
-    for (int u = 0; u < 4; ++u)
+    for (int u = 0; u < PER; ++u)
       if (off[u] >= 0) *reinterpret_cast<uint4*>(buf + off[u]) = v[u];
   }
 }
 
+struct Maps {
+  CUtensorMap wlat, wg, wu, wd, mix;
+};
+
 template <int MTILES>
 __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1) latent_mma_kernel(
-    const int64_t* __restrict__ blk, const int64_t* __restrict__ am1, const float* __restrict__ xh,
-    const bf16* __restrict__ w1, const bf16* __restrict__ wlat, const float* __restrict__ mixT,
-    const bf16* __restrict__ wg, const bf16* __restrict__ wu, const bf16* __restrict__ wd,
+    const __grid_constant__ Maps maps, const int64_t* __restrict__ blk,
+    const int64_t* __restrict__ am1, const float* __restrict__ xh, const bf16* __restrict__ w1,
     bf16* __restrict__ lat, int N, int B, int r, int H, int V, uint32_t* err) {
   constexpr int MT = MTILES * 16;
   constexpr int MAXU = (MT * 32 + THREADS - 1) / THREADS;   // outputs per thread, CS <= 32
-  extern __shared__ __align__(128) uint8_t sm[];
+  extern __shared__ uint8_t sm_raw[];
+  uint8_t* sm = sm_raw + ((1024u - (ptx::smem_u32(sm_raw) & 1023u)) & 1023u);
   cg::cluster_group cluster = cg::this_cluster();
   const int q = (int)cluster.block_rank();
   const int cid = blockIdx.x / CL, nclusters = gridDim.x / CL;
-  const Plan P = make_plan(MT, r, H);
+  const Plan P = make_plan(MT, r, H, B);
   const int CS = P.CS, HS = P.HS;
-  bf16* sWl = (bf16*)(sm + P.wlat);
-  bf16* sWg = (bf16*)(sm + P.wg);
-  bf16* sWu = (bf16*)(sm + P.wu);
-  bf16* sWd = (bf16*)(sm + P.wd);
-  bf16* sU = (bf16*)(sm + P.ufull);
-  bf16* sA = (bf16*)(sm + P.afull);        // embeddings first, activations later
+  const uint32_t s0 = ptx::smem_u32(sm);
+  const uint32_t aWl = s0 + P.wlat, aWg = s0 + P.wg, aWu = s0 + P.wu, aWd = s0 + P.wd;
+  const uint32_t aEA = s0 + P.ea, aU = s0 + P.u;
+  const bf16* sMix = (const bf16*)(sm + P.mix);
+  const float* sXh = (const float*)(sm + P.xh);
   float* sPart = (float*)(sm + P.part);
   float* sUs = (float*)(sm + P.us);
   int64_t* sPrev = (int64_t*)(sm + P.prev);
+  const uint32_t bar = s0 + P.bar;
+  int& s_abort = *reinterpret_cast<int*>(sm + P.bar + 8);   // beside the mbarrier
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   const int g8 = lane / 4, t4 = lane % 4;
   const int nb = MT / B;                   // blocks per group
   const int groups = (N + nb - 1) / nb;
   const int ldp = CS + 1;
 
-  // ---- weight slices -> smem, once (nothing here depends on the previous pass) ----
-  {
-    auto stage = [&](bf16* dst, int pitch, const bf16* src, int nrows, int ncols) {
-      const int chunks = ncols / 8;
-      for (int i = tid; i < nrows * chunks; i += THREADS) {
-        const int rr = i / chunks, cc = i % chunks;
-        cp_async16(dst + rr * pitch + cc * 8, src + (int64_t)rr * ncols + cc * 8);
-      }
-    };
-    stage(sWl, P.pk_r, wlat + (int64_t)q * CS * r, CS, r);
-    stage(sWg, P.pk_r, wg + (int64_t)q * HS * r, HS, r);
-    stage(sWu, P.pk_r, wu + (int64_t)q * HS * r, HS, r);
-    stage(sWd, P.pk_h, wd + (int64_t)q * CS * H, CS, H);
+  // ---- weight and mixer slices by TMA, once: nothing here depends on the previous pass ----
+  if (tid == 0) {
+    s_abort = 0;
+    ptx::mbar_init(bar, 1);
+    ptx::fence_barrier_init();
+    const int wbytes = (CS * r + 2 * HS * r + CS * H) * 2;
+    const int mparts = (P.mix_rows + 255) / 256;
+    ptx::mbar_arrive_expect_tx(bar, wbytes + mparts * std::min(P.mix_rows, 256) * CS * 2);
+    const uint64_t pol = ptx::policy_evict_last();
+    for (int kc = 0; kc < r / 64; ++kc) {
+      ptx::tma_load_2d(aWl + kc * CS * 128, &maps.wlat, bar, kc * 64, q * CS, pol);
+      ptx::tma_load_2d(aWg + kc * HS * 128, &maps.wg, bar, kc * 64, q * HS, pol);
+      ptx::tma_load_2d(aWu + kc * HS * 128, &maps.wu, bar, kc * 64, q * HS, pol);
+    }
+    for (int kc = 0; kc < H / 64; ++kc)
+      ptx::tma_load_2d(aWd + kc * CS * 128, &maps.wd, bar, kc * 64, q * CS, pol);
+    for (int pt = 0; pt < mparts; ++pt)
+      ptx::tma_load_2d(s0 + P.mix + pt * 256 * CS * 2, &maps.mix, bar, q * CS, pt * 256, pol);
   }
-  pdl_wait();                              // blk (and xh) come from earlier kernels
-  pdl_trigger();
+  ptx::pdl_wait();                         // blk (and xh) come from earlier kernels
+  ptx::pdl_trigger();
+  __syncthreads();
+  if (tid == 0 && !ptx::mbar_wait(bar, 0, &s_abort, err)) s_abort = 1;
+  __syncthreads();
 
   for (int grp = cid; grp < groups; grp += nclusters) {
     const int n0 = grp * nb;
     const int rows = std::min(nb, N - n0) * B;   // valid rows of this group
 
-    // ---- token ids and embeddings ----
+    // ---- token ids, then embeddings and the xh slice by cp.async ----
     for (int m = tid; m < MT; m += THREADS) {
       int64_t t = 0;
       if (m < rows) {
@@ -223,13 +255,23 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1) latent_
     }
     __syncthreads();
     {
-      const int chunks = r / 8;
-      for (int i = tid; i < MT * chunks; i += THREADS) {
-        const int m = i / chunks, cc = i % chunks;
-        if (m < rows)
-          cp_async16(sA + m * P.pk_r + cc * 8, w1 + sPrev[m] * r + cc * 8);
-        else
-          *reinterpret_cast<uint4*>(sA + m * P.pk_r + cc * 8) = make_uint4(0, 0, 0, 0);
+      const int ec = r / 8, xc = CS / 4;
+      for (int i = tid; i < MT * (ec + xc); i += THREADS) {
+        const int m = i / (ec + xc), c = i % (ec + xc);
+        if (c < ec) {
+          const uint32_t dst = aEA + swz(m, c * 8, MT);
+          if (m < rows)
+            cp_async16(dst, w1 + sPrev[m] * r + c * 8);
+          else
+            *reinterpret_cast<uint4*>(sm + (dst - s0)) = make_uint4(0, 0, 0, 0);
+        } else {
+          const int cc = c - ec;
+          const uint32_t dst = s0 + P.xh + (m * CS + cc * 4) * 4;
+          if (m < rows)
+            cp_async16(dst, xh + ((int64_t)(n0 * B + m)) * r + q * CS + cc * 4);
+          else
+            *reinterpret_cast<uint4*>(sm + (dst - s0)) = make_uint4(0, 0, 0, 0);
+        }
       }
     }
     cp_async_wait_all();
@@ -240,7 +282,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1) latent_
       const int nt = warp % P.nt1, ks = warp / P.nt1;
       const int kl = r / P.ks1;
       float acc[MTILES][4] = {};
-      warp_gemm<MTILES>(acc, sA, P.pk_r, sWl, P.pk_r, nt * 8, ks * kl, (ks + 1) * kl);
+      warp_gemm<MTILES>(acc, aEA, aWl, CS, nt * 8, ks * kl, (ks + 1) * kl);
       float* dst = sPart + ks * MT * ldp;
 #pragma unroll
       for (int i = 0; i < MTILES; ++i)
@@ -249,19 +291,19 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1) latent_
           dst[(i * 16 + g8 + (e >= 2 ? 8 : 0)) * ldp + nt * 8 + 2 * t4 + (e & 1)] = acc[i][e];
     }
     __syncthreads();
-    for (int i = tid; i < MT * CS; i += THREADS) {
-      const int m = i / CS, c = i % CS;
-      float x = 0.f;
-      if (m < rows) {
-        x = xh[((int64_t)(n0 * B + m)) * r + q * CS + c];
+#pragma unroll
+    for (int k = 0; k < MAXU; ++k) {
+      const int i = tid + k * THREADS;
+      if (i < MT * CS) {
+        const int m = i / CS, c = i % CS;
+        float x = sXh[m * CS + c];
         for (int ks = 0; ks < P.ks1; ++ks) x += sPart[ks * MT * ldp + m * ldp + c];
+        sUs[m * ldp + c] = x;
       }
-      sUs[m * ldp + c] = x;
     }
     __syncthreads();
 
     // ---- causal per-channel mixer (fp32): u[b, c] = sum_j mix[c, b, j] x[j, c] ----
-    // mixT is the folded mixer laid out [b][j][channel] (fp32): coalesced reads.
     float uval[MAXU];
 #pragma unroll
     for (int k = 0; k < MAXU; ++k) {
@@ -270,9 +312,9 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1) latent_
       float u = 0.f;
       if (i < MT * CS && m < rows) {
         const int bl = m / B, b = m % B;
-        const float* mc = mixT + (int64_t)b * B * r + q * CS + c;
+        const bf16* mc = sMix + (b * B) * CS + c;      // rows (b, j), columns = channels
         for (int j = 0; j < B; ++j)
-          u = fmaf(__ldg(mc + (int64_t)j * r), sUs[(bl * B + j) * ldp + c], u);
+          u = fmaf(__bfloat162float(mc[j * CS]), sUs[(bl * B + j) * ldp + c], u);
       }
       uval[k] = u;
     }
@@ -283,28 +325,29 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1) latent_
       if (i < MT * CS) {
         const int m = i / CS, c = i % CS;
         sUs[m * ldp + c] = uval[k];
-        sU[m * P.pk_r + q * CS + c] = __float2bfloat16_rn(uval[k]);
+        *reinterpret_cast<bf16*>(sm + P.u + swz(m, q * CS + c, MT)) = __float2bfloat16_rn(uval[k]);
       }
     }
     cluster.sync();
-    gather_peers(cluster, sU, MT, P.pk_r, CS, q);
+    gather_peers<MTILES, 6>(cluster, sm + P.u, CS, q);
     __syncthreads();
 
     // ---- phase 2: SwiGLU on own hidden units: a = silu(u w_gate^T) * (u w_up^T) ----
     for (int nt = warp; nt < HS / 8; nt += NW) {
       float ag[MTILES][4] = {}, au[MTILES][4] = {};
-      warp_gemm_pair<MTILES>(ag, au, sU, P.pk_r, sWg, sWu, P.pk_r, nt * 8, r);
+      warp_gemm_pair<MTILES>(ag, au, aU, aWg, aWu, HS, nt * 8, r);
 #pragma unroll
       for (int i = 0; i < MTILES; ++i)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int m = i * 16 + g8 + (e >= 2 ? 8 : 0);
-          const int hh = nt * 8 + 2 * t4 + (e & 1);
-          sA[m * P.pk_h + q * HS + hh] = __float2bfloat16_rn(silu(ag[i][e]) * au[i][e]);
+          const int hh = q * HS + nt * 8 + 2 * t4 + (e & 1);
+          *reinterpret_cast<bf16*>(sm + P.ea + swz(m, hh, MT)) =
+              __float2bfloat16_rn(silu(ag[i][e]) * au[i][e]);
         }
     }
     cluster.sync();
-    gather_peers(cluster, sA, MT, P.pk_h, HS, q);
+    gather_peers<MTILES, 11>(cluster, sm + P.ea, HS, q);
     __syncthreads();
 
     // ---- phase 3: lat (own channels) = u + a . w_down^T, K split over warp groups ----
@@ -312,7 +355,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1) latent_
       const int nt = warp % P.nt1, ks = warp / P.nt1;
       const int kl = H / P.ks1;
       float acc[MTILES][4] = {};
-      warp_gemm<MTILES>(acc, sA, P.pk_h, sWd, P.pk_h, nt * 8, ks * kl, (ks + 1) * kl);
+      warp_gemm<MTILES>(acc, aEA, aWd, CS, nt * 8, ks * kl, (ks + 1) * kl);
       float* dst = sPart + ks * MT * ldp;
 #pragma unroll
       for (int i = 0; i < MTILES; ++i)
@@ -321,16 +364,25 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1) latent_
           dst[(i * 16 + g8 + (e >= 2 ? 8 : 0)) * ldp + nt * 8 + 2 * t4 + (e & 1)] = acc[i][e];
     }
     __syncthreads();
-    for (int i = tid; i < MT * CS; i += THREADS) {
-      const int m = i / CS, c = i % CS;
-      if (m < rows && (m % B) != 0) {
-        float v = sUs[m * ldp + c];
-        for (int ks = 0; ks < P.ks1; ++ks) v += sPart[ks * MT * ldp + m * ldp + c];
-        const int n = n0 + m / B, b = m % B;
-        lat[((int64_t)n * (B - 1) + b - 1) * r + q * CS + c] = __float2bfloat16_rn(v);
+#pragma unroll
+    for (int k = 0; k < MAXU; ++k) {
+      const int i = tid + k * THREADS;
+      if (i < MT * CS) {
+        const int m = i / CS, c = i % CS;
+        if (m < rows && (m % B) != 0) {
+          float v = sUs[m * ldp + c];
+          for (int ks = 0; ks < P.ks1; ++ks) v += sPart[ks * MT * ldp + m * ldp + c];
+          const int n = n0 + m / B, b = m % B;
+          lat[((int64_t)n * (B - 1) + b - 1) * r + q * CS + c] = __float2bfloat16_rn(v);
+        }
       }
     }
     cluster.sync();   // peers may still read this CTA's u / activation slices
+  }
+  // nothing may land in shared memory after the CTA exits
+  if (tid == 0 && s_abort) {
+    volatile int no_abort = 0;
+    ptx::mbar_wait(bar, 0, &no_abort, err);
   }
 }
 
@@ -353,20 +405,23 @@ int max_clusters(int smem) {
   return n;
 }
 
+size_t smem_bytes(int MT, int r, int H, int B) { return (size_t)make_plan(MT, r, H, B).total + 1024; }
+
 template <int MTILES>
 cudaError_t launch(const xp_head* h, const int64_t* blk, const int64_t* am1, const float* xh,
                    int N, void* lat, cudaStream_t s) {
-  const Plan P = make_plan(MTILES * 16, h->r, h->H);
+  const Plan P = make_plan(MTILES * 16, h->r, h->H, h->B);
+  const int smem = (int)smem_bytes(P.MT, h->r, h->H, h->B);
   cudaError_t e = cudaFuncSetAttribute(latent_mma_kernel<MTILES>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, P.total);
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int nb = P.MT / h->B;
   const int groups = (N + nb - 1) / nb;
-  const int clusters = std::min(groups, max_clusters<MTILES>(P.total));
-  e = xp_launch_pdl(latent_mma_kernel<MTILES>, dim3(clusters * CL), dim3(THREADS),
-                    (size_t)P.total, s, blk, am1, xh, (const bf16*)h->w1, (const bf16*)h->w_lat,
-                    (const float*)h->mixT, (const bf16*)h->w_gate, (const bf16*)h->w_up,
-                    (const bf16*)h->w_down, (bf16*)lat, N, h->B, h->r, h->H, h->V, h->err);
+  const int clusters = std::min(groups, max_clusters<MTILES>(smem));
+  const Maps maps = {h->tm_wlat, h->tm_wg, h->tm_wu, h->tm_wd, h->tm_mixT};
+  e = xp_launch_pdl(latent_mma_kernel<MTILES>, dim3(clusters * CL), dim3(THREADS), (size_t)smem,
+                    s, maps, blk, am1, xh, (const bf16*)h->w1, (bf16*)lat, N, h->B, h->r, h->H,
+                    h->V, h->err);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
@@ -376,14 +431,38 @@ bool xp_latent_mma_ok(int r, int H, int B, xp_dtype dt) {
   if (dt != XP_BF16 || B < 2 || B > 32) return false;
   if (r != 64 && r != 128 && r != 256) return false;      // r/8 channels = 1, 2 or 4 n-tiles
   if (H % (8 * CL) != 0 || H > 1024) return false;
-  return make_plan(48, r, H).total <= 227 * 1024;
+  return smem_bytes(48, r, H, B) <= 227 * 1024;
+}
+
+// Tensor maps of the weight and mixer slices (2-D, bf16; weights 128B-swizzled).
+bool xp_latent_mma_maps(xp_head* h) {
+  xp_encode_tiled_fn fn = xp_get_encode_tiled();
+  if (!fn) return false;
+  const int r = h->r, H = h->H, B = h->B, CS = r / CL, HS = H / CL;
+  auto enc = [&](CUtensorMap* m, const void* ptr, int rows, int cols, int box_c, int box_r,
+                 bool swz128) {
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)box_c, (cuuint32_t)box_r};
+    const cuuint32_t es[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+              es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              swz128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+  };
+  return enc(&h->tm_wlat, h->w_lat, r, r, 64, CS, true) &&
+         enc(&h->tm_wg, h->w_gate, H, r, 64, HS, true) &&
+         enc(&h->tm_wu, h->w_up, H, r, 64, HS, true) &&
+         enc(&h->tm_wd, h->w_down, r, H, 64, CS, true) &&
+         enc(&h->tm_mixT, h->mixT, B * B, r, CS, std::min(B * B, 256), false);
 }
 
 cudaError_t xp_launch_latent_mma(const xp_head* h, const int64_t* blk, const int64_t* am1,
                                  const float* xh, int N, void* lat, cudaStream_t s) {
   // 32-row groups while they fit in one wave of co-resident clusters, else 48-row groups
-  const Plan p32 = make_plan(32, h->r, h->H);
   const int groups32 = (N + 32 / h->B - 1) / (32 / h->B);
-  if (groups32 <= max_clusters<2>(p32.total)) return launch<2>(h, blk, am1, xh, N, lat, s);
+  if (groups32 <= max_clusters<2>((int)smem_bytes(32, h->r, h->H, h->B)))
+    return launch<2>(h, blk, am1, xh, N, lat, s);
   return launch<3>(h, blk, am1, xh, N, lat, s);
 }

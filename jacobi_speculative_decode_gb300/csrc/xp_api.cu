@@ -43,7 +43,7 @@ PrepLayout prep_layout(const xp_weights* w) {
   L.w_hc = take(r * 2 * r * es);
   L.w_lat = take(r * r * es);
   L.mix = take(r * B * B * es);
-  L.mixT = take(r * B * B * 4);
+  L.mixT = take(r * B * B * es);
   L.w_gate = take(H * r * es);
   L.w_up = take(H * r * es);
   L.w_down = take(r * H * es);
@@ -172,7 +172,7 @@ xp_status xp_head_create(const xp_weights* w, void* prep_dev, size_t prep_bytes,
   h->err = (uint32_t*)(p + L.err);
   h->w1 = p + L.w1; h->down_hg = p + L.down_hg;
   h->w_hc = p + L.w_hc; h->w_lat = p + L.w_lat; h->mix = p + L.mix;
-  h->mixT = (float*)(p + L.mixT);
+  h->mixT = p + L.mixT;
   h->w_gate = p + L.w_gate; h->w_up = p + L.w_up; h->w_down = p + L.w_down; h->w2 = p + L.w2;
   xp_status st = copy_weights(h, w, stream);
   if (st == XP_OK) st = cuda_status(cudaMemsetAsync(h->err, 0, 256, stream));
@@ -368,7 +368,7 @@ static void decide_paths(xp_head* h) {
   cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, h->device);
   const bool blackwell = major == 10 && minor == 3;
   if (!blackwell || h->dtype != XP_BF16) return;
-  h->latent_mma = xp_latent_mma_ok(h->r, h->H, h->B, h->dtype) ? 1 : 0;
+  h->latent_mma = xp_latent_mma_ok(h->r, h->H, h->B, h->dtype) && xp_latent_mma_maps(h);
   // tcgen05 readout: K = r tiled by 64-wide (128-byte) swizzled chunks, at most 4
   // of them resident; draft rows of one block never straddle a 128-row tile
   if (h->r % 64 == 0 && h->r <= 256 && h->B - 1 <= 128 && xp_get_encode_tiled()) {

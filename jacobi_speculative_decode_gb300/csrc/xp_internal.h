@@ -17,10 +17,11 @@ struct xp_head {
   size_t prep_bytes;
   uint32_t* err;         // device error word (XP_ERR_* bits)
   void *w1, *down_hg, *w_hc, *w_lat, *mix, *w_gate, *w_up, *w_down, *w2;  // down_hg = [down_h ; down_g]
-  float* mixT;           // folded mixer as fp32 [out slot][in slot][channel]
+  void* mixT;            // folded mixer laid out [out slot][in slot][channel]
   int readout_tc;        // tcgen05 readout usable for this head's shapes
   int latent_mma;        // cluster tensor-core latent usable for this head's shapes
   CUtensorMap tm_w2;     // W2 [V, r] tiled map for the tcgen05 readout
+  CUtensorMap tm_wlat, tm_wg, tm_wu, tm_wd, tm_mixT;   // latent weight slices (TMA)
 };
 
 // device error word bits
@@ -43,7 +44,7 @@ static inline size_t xp_elem(xp_dtype d) { return d == XP_BF16 ? 2 : 4; }
 
 // ---- launchers (return cudaGetLastError() after launching) -----------------
 cudaError_t xp_launch_fold(const void* raw, void* mix, int r, int B, xp_dtype dt, cudaStream_t s);
-cudaError_t xp_launch_mix_transpose(const void* mix, float* mixT, int r, int B, xp_dtype dt,
+cudaError_t xp_launch_mix_transpose(const void* mix, void* mixT, int r, int B, xp_dtype dt,
                                     cudaStream_t s);
 
 cudaError_t xp_launch_hidden(const xp_head* h, const void* h_full, int N, float* xh, float* part,
@@ -56,6 +57,7 @@ cudaError_t xp_launch_init_argmax(const xp_head* h, const void* base, int64_t sn
 cudaError_t xp_launch_latent_simt(const xp_head* h, const int64_t* blk, const int64_t* am1,
                                   const float* xh, int N, void* lat, cudaStream_t s);
 bool xp_latent_mma_ok(int r, int H, int B, xp_dtype dt);
+bool xp_latent_mma_maps(xp_head* h);
 cudaError_t xp_launch_latent_mma(const xp_head* h, const int64_t* blk, const int64_t* am1,
                                  const float* xh, int N, void* lat, cudaStream_t s);
 

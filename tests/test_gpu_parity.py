@@ -259,3 +259,20 @@ def test_capacity_and_validation(case):
     assert e.value.code == xp.XP_EINVAL
     # zero blocks is a no-op
     xp.xp_readout_argmax(dev.head.handle, dev.base, dev.base, dev.sn, dev.sb, 0, blk, None, dev.ws)
+
+
+def test_latent_persistent_many_groups():
+    # more row groups than co-resident clusters: every cluster walks several groups
+    wl = I.workload("batched-decode", V=4096, hidden=64, N=300, K=1)
+    d = I.make_inputs(wl)
+    dev = Dev(d, wl)
+    p = O.params_from_inputs(d, wl.dtype)
+    xh_np = I.random_xh(wl, seed=5)
+    lat = torch.empty(wl.N, wl.B - 1, wl.r, dtype=torch.bfloat16, device="cuda")
+    for _ in range(2):                       # twice: the second call reuses warm state
+        xp.xp_latent_pass(dev.head.handle, dev.blk_in, dev.am1, torch.from_numpy(xh_np).cuda(),
+                          wl.N, lat)
+    assert xp.xp_get_error(dev.head.handle) == xp.XP_OK
+    want = O.latent(d["blk"], d["am1"], xh_np.astype(np.float64), p)
+    check_close(O.decode(xp.to_host_storage(lat), "bf16"), want, LAT_TOL["bf16"], "lat")
+    dev.close()
