@@ -149,7 +149,9 @@ def run_native(args, rank, world, local):
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
+    from jacobi_speculative_decode_gb300 import shard
     wl = I.workload(args.workload)
+    wl = I.workload(args.workload, seed=shard.rank_seed(wl.seed, rank))   # this rank's own batch
     d = I.make_inputs(wl)
     head, _ = xp.head_from_inputs(d, wl)
     base = xp.to_device(d["base"], wl.dtype)
@@ -184,12 +186,7 @@ def run_native(args, rank, world, local):
             step()
         e1.record(stream)
         barrier()
-    ms = e0.elapsed_time(e1)
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = shard.max_over_ranks(e0.elapsed_time(e1), device=dev)
     status = xp.xp_get_error(head.handle)
     if status != xp.XP_OK:
         raise RuntimeError(f"device error in the timed region: {xp.status_str(status)}")

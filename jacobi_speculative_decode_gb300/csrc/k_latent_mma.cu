@@ -10,11 +10,16 @@
 // w_down products and hidden units [q*H/8, (q+1)*H/8) of the SwiGLU.  Its
 // weight and mixer slices arrive by TMA once, before the kernel waits on the
 // previous pass, and stay in shared memory while the cluster walks over groups
-// of MT rows (whole blocks).  Per group the embeddings and the xh slice arrive
-// by cp.async; the full u and SwiGLU activations are exchanged through
-// distributed shared memory.  Products use mma.sync m16n8k16 (bf16 in, fp32
-// accumulate); the mixer, the K-split partial sums (added in a fixed order)
-// and the residual stay in fp32.
+// of 32 rows (whole blocks).  Per group the embeddings and the xh slice arrive
+// by cp.async.  Products use mma.sync m16n8k16 (bf16 in, fp32 accumulate):
+//   x slice   = emb . w_lat[own channels]^T
+//   u         = per-channel causal mix of x (fp32); the full u is exchanged over
+//               distributed shared memory as a bf16 hi + lo pair (u = hi + lo to
+//               ~2^-17), so the SwiGLU sees u, not bf16(u)
+//   a slice   = silu(u . w_gate[own units]^T) * (u . w_up[own units]^T), kept as hi + lo
+//   partial   = a slice . w_down[:, own units]^T for ALL r channels (a K split)
+//   lat       = u + sum over the 8 CTAs of their partials for the own channels,
+//               added in a fixed order (deterministic), read over DSMEM.
 //
 // Every bf16 matrix in shared memory uses the TMA 128-byte-swizzle layout in
 // 64-column chunks: element (row, k) of an R-row matrix lives at
@@ -38,22 +43,25 @@ constexpr int THREADS = 256;   // 8 warps
 constexpr int NW = THREADS / 32;
 
 struct Plan {                  // shapes and byte offsets into dynamic shared memory
-  int MT, CS, HS;
-  int nt1, ks1;                // in_proj / w_down: n-tiles of the CTA's channels, K splits
-  int wlat, wg, wu, wd, mix, ea, u, xh, part, us, prev, bar;
-  int mix_rows;                // B*B
+  int CS, HS;
+  int nt1, ks1;                // in_proj: n-tiles of the CTA's channels, K splits
+  int wlat, wg, wu, wdk, mix, ep, uhi, ulo, ahi, alo, xh, part, us, prev, bar;
+  int mix_rows, pp;            // B*B; pitch (floats) of the fp32 partial sums
   int total;
 };
 
-__host__ __device__ inline Plan make_plan(int MT, int r, int H, int B) {
+constexpr int MTILES = 2;
+constexpr int MT = MTILES * 16; // rows per group
+
+__host__ __device__ inline Plan make_plan(int r, int H, int B) {
   Plan p;
-  p.MT = MT;
   p.CS = r / CL;
   p.HS = H / CL;
   p.nt1 = p.CS / 8;
   // K splits: fill the warps, keep every split a whole number of 16-wide k-steps
-  p.ks1 = std::min(NW / p.nt1, std::min(r, H) / 16);
+  p.ks1 = std::min(NW / p.nt1, r / 16);
   p.mix_rows = B * B;
+  p.pp = r + 4;
   const int mparts = (p.mix_rows + 255) / 256, mbox = std::min(p.mix_rows, 256);
   int o = 0;
   // TMA / swizzled regions 1024-byte aligned, the rest 16-byte aligned
@@ -66,10 +74,13 @@ __host__ __device__ inline Plan make_plan(int MT, int r, int H, int B) {
   p.wlat = take(p.CS * r * 2, 1024);
   p.wg = take(p.HS * r * 2, 1024);
   p.wu = take(p.HS * r * 2, 1024);
-  p.wd = take(p.CS * H * 2, 1024);
+  p.wdk = take(r * p.HS * 2, 1024);          // w_down[:, own units]: r rows x HS
   p.mix = take(mparts * mbox * p.CS * 2, 1024);
-  p.ea = take(MT * std::max(r, H) * 2, 1024);   // embeddings, later the activations
-  p.u = take(MT * r * 2, 1024);
+  p.ep = take(std::max(MT * r * 2, MT * p.pp * 4), 1024);   // embeddings, later partials
+  p.uhi = take(MT * r * 2, 1024);
+  p.ulo = take(MT * r * 2, 1024);
+  p.ahi = take(MT * p.HS * 2, 1024);
+  p.alo = take(MT * p.HS * 2, 1024);
   p.xh = take(MT * p.CS * 4, 16);
   p.part = take(p.ks1 * MT * (p.CS + 1) * 4, 16);
   p.us = take(MT * (p.CS + 1) * 4, 16);
@@ -152,58 +163,67 @@ __device__ __forceinline__ void warp_gemm_pair(float (&acc0)[MTILES][4], float (
   }
 }
 
-// Copy the columns [p*W, (p+1)*W) of a swizzled MT-row matrix from every other CTA p of
-// the cluster into this CTA's copy (same offsets everywhere); all loads issued first.
-template <int MTILES, int PER>
-__device__ __forceinline__ void gather_peers(cg::cluster_group& cluster, uint8_t* buf, int W,
-                                             int q) {
-  constexpr int MT = MTILES * 16;
+// Copy the columns [p*W, (p+1)*W) of two swizzled MT-row matrices from every other CTA p
+// of the cluster into this CTA's copies (same offsets everywhere); loads issued first.
+template <int PER>
+__device__ __forceinline__ void gather_peers2(cg::cluster_group& cluster, uint8_t* b0, uint8_t* b1,
+                                              int W, int q) {
   const int chunks = W / 8;                       // 16-byte chunks per row and peer
-  const int total = (CL - 1) * MT * chunks;
+  const int per_buf = (CL - 1) * MT * chunks;
+  const int total = 2 * per_buf;
   for (int i0 = threadIdx.x; i0 < total; i0 += PER * THREADS) {
     uint4 v[PER];
     int off[PER];
+    uint8_t* dst[PER];
 #pragma unroll
     for (int u = 0; u < PER; ++u) {
       const int i = i0 + u * THREADS;
       off[u] = -1;
       if (i < total) {
-        const int pp = i / (MT * chunks), rem = i % (MT * chunks);
+        const int which = i / per_buf, j = i % per_buf;
+        const int pp = j / (MT * chunks), rem = j % (MT * chunks);
         const int p = pp + (pp >= q);
         const int m = rem / chunks, cc = rem % chunks;
         off[u] = swz(m, p * W + cc * 8, MT);
-        v[u] = *reinterpret_cast<const uint4*>(cluster.map_shared_rank(buf, p) + off[u]);
+        dst[u] = which ? b1 : b0;
+        v[u] = *reinterpret_cast<const uint4*>(cluster.map_shared_rank(dst[u], p) + off[u]);
       }
     }
 #pragma unroll
     for (int u = 0; u < PER; ++u)
-      if (off[u] >= 0) *reinterpret_cast<uint4*>(buf + off[u]) = v[u];
+      if (off[u] >= 0) *reinterpret_cast<uint4*>(dst[u] + off[u]) = v[u];
   }
 }
 
+__device__ __forceinline__ void split_store(uint8_t* hi, uint8_t* lo, int off, float v) {
+  const bf16 h = __float2bfloat16_rn(v);
+  *reinterpret_cast<bf16*>(hi + off) = h;
+  *reinterpret_cast<bf16*>(lo + off) = __float2bfloat16_rn(v - __bfloat162float(h));
+}
+
 struct Maps {
-  CUtensorMap wlat, wg, wu, wd, mix;
+  CUtensorMap wlat, wg, wu, wdk, mix;
 };
 
-template <int MTILES>
 __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1) latent_mma_kernel(
     const __grid_constant__ Maps maps, const int64_t* __restrict__ blk,
     const int64_t* __restrict__ am1, const float* __restrict__ xh, const bf16* __restrict__ w1,
     bf16* __restrict__ lat, int N, int B, int r, int H, int V, uint32_t* err) {
-  constexpr int MT = MTILES * 16;
   constexpr int MAXU = (MT * 32 + THREADS - 1) / THREADS;   // outputs per thread, CS <= 32
   extern __shared__ uint8_t sm_raw[];
   uint8_t* sm = sm_raw + ((1024u - (ptx::smem_u32(sm_raw) & 1023u)) & 1023u);
   cg::cluster_group cluster = cg::this_cluster();
   const int q = (int)cluster.block_rank();
   const int cid = blockIdx.x / CL, nclusters = gridDim.x / CL;
-  const Plan P = make_plan(MT, r, H, B);
+  const Plan P = make_plan(r, H, B);
   const int CS = P.CS, HS = P.HS;
   const uint32_t s0 = ptx::smem_u32(sm);
-  const uint32_t aWl = s0 + P.wlat, aWg = s0 + P.wg, aWu = s0 + P.wu, aWd = s0 + P.wd;
-  const uint32_t aEA = s0 + P.ea, aU = s0 + P.u;
+  const uint32_t aWl = s0 + P.wlat, aWg = s0 + P.wg, aWu = s0 + P.wu, aWdk = s0 + P.wdk;
+  const uint32_t aE = s0 + P.ep, aUhi = s0 + P.uhi, aUlo = s0 + P.ulo;
+  const uint32_t aAhi = s0 + P.ahi, aAlo = s0 + P.alo;
   const bf16* sMix = (const bf16*)(sm + P.mix);
   const float* sXh = (const float*)(sm + P.xh);
+  float* sP = (float*)(sm + P.ep);          // partial sums of the down projection [MT][pp]
   float* sPart = (float*)(sm + P.part);
   float* sUs = (float*)(sm + P.us);
   int64_t* sPrev = (int64_t*)(sm + P.prev);
@@ -220,19 +240,22 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1) latent_
     s_abort = 0;
     ptx::mbar_init(bar, 1);
     ptx::fence_barrier_init();
-    const int wbytes = (CS * r + 2 * HS * r + CS * H) * 2;
-    const int mparts = (P.mix_rows + 255) / 256;
-    ptx::mbar_arrive_expect_tx(bar, wbytes + mparts * std::min(P.mix_rows, 256) * CS * 2);
+    const int wbytes = (CS * r + 2 * HS * r + r * HS) * 2;
+    const int mparts = (P.mix_rows + 255) / 256, mbox = std::min(P.mix_rows, 256);
+    const int rparts = (r + 255) / 256, rbox = std::min(r, 256);
+    ptx::mbar_arrive_expect_tx(bar, wbytes + mparts * mbox * CS * 2);
     const uint64_t pol = ptx::policy_evict_last();
     for (int kc = 0; kc < r / 64; ++kc) {
       ptx::tma_load_2d(aWl + kc * CS * 128, &maps.wlat, bar, kc * 64, q * CS, pol);
       ptx::tma_load_2d(aWg + kc * HS * 128, &maps.wg, bar, kc * 64, q * HS, pol);
       ptx::tma_load_2d(aWu + kc * HS * 128, &maps.wu, bar, kc * 64, q * HS, pol);
     }
-    for (int kc = 0; kc < H / 64; ++kc)
-      ptx::tma_load_2d(aWd + kc * CS * 128, &maps.wd, bar, kc * 64, q * CS, pol);
+    for (int kc = 0; kc < HS / 64; ++kc)
+      for (int rp = 0; rp < rparts; ++rp)
+        ptx::tma_load_2d(aWdk + (kc * r + rp * rbox) * 128, &maps.wdk, bar, q * HS + kc * 64,
+                         rp * rbox, pol);
     for (int pt = 0; pt < mparts; ++pt)
-      ptx::tma_load_2d(s0 + P.mix + pt * 256 * CS * 2, &maps.mix, bar, q * CS, pt * 256, pol);
+      ptx::tma_load_2d(s0 + P.mix + pt * mbox * CS * 2, &maps.mix, bar, q * CS, pt * mbox, pol);
   }
   ptx::pdl_wait();                         // blk (and xh) come from earlier kernels
   ptx::pdl_trigger();
@@ -259,7 +282,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1) latent_
       for (int i = tid; i < MT * (ec + xc); i += THREADS) {
         const int m = i / (ec + xc), c = i % (ec + xc);
         if (c < ec) {
-          const uint32_t dst = aEA + swz(m, c * 8, MT);
+          const uint32_t dst = aE + swz(m, c * 8, MT);
           if (m < rows)
             cp_async16(dst, w1 + sPrev[m] * r + c * 8);
           else
@@ -277,12 +300,12 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1) latent_
     cp_async_wait_all();
     __syncthreads();
 
-    // ---- phase 1: x (own channels) = xh + emb . w_lat^T, K split over warp groups ----
+    // ---- x (own channels) = xh + emb . w_lat^T, K split over warp groups ----
     if (warp < P.nt1 * P.ks1) {
       const int nt = warp % P.nt1, ks = warp / P.nt1;
       const int kl = r / P.ks1;
       float acc[MTILES][4] = {};
-      warp_gemm<MTILES>(acc, aEA, aWl, CS, nt * 8, ks * kl, (ks + 1) * kl);
+      warp_gemm<MTILES>(acc, aE, aWl, CS, nt * 8, ks * kl, (ks + 1) * kl);
       float* dst = sPart + ks * MT * ldp;
 #pragma unroll
       for (int i = 0; i < MTILES; ++i)
@@ -325,59 +348,62 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1) latent_
       if (i < MT * CS) {
         const int m = i / CS, c = i % CS;
         sUs[m * ldp + c] = uval[k];
-        *reinterpret_cast<bf16*>(sm + P.u + swz(m, q * CS + c, MT)) = __float2bfloat16_rn(uval[k]);
+        split_store(sm + P.uhi, sm + P.ulo, swz(m, q * CS + c, MT), uval[k]);
       }
     }
     cluster.sync();
-    gather_peers<MTILES, 6>(cluster, sm + P.u, CS, q);
+    gather_peers2<7>(cluster, sm + P.uhi, sm + P.ulo, CS, q);
     __syncthreads();
 
-    // ---- phase 2: SwiGLU on own hidden units: a = silu(u w_gate^T) * (u w_up^T) ----
+    // ---- SwiGLU on own hidden units, from u = hi + lo: a = silu(u w_g^T) * (u w_u^T) ----
     for (int nt = warp; nt < HS / 8; nt += NW) {
       float ag[MTILES][4] = {}, au[MTILES][4] = {};
-      warp_gemm_pair<MTILES>(ag, au, aU, aWg, aWu, HS, nt * 8, r);
+      warp_gemm_pair<MTILES>(ag, au, aUhi, aWg, aWu, HS, nt * 8, r);
+      warp_gemm_pair<MTILES>(ag, au, aUlo, aWg, aWu, HS, nt * 8, r);
 #pragma unroll
       for (int i = 0; i < MTILES; ++i)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int m = i * 16 + g8 + (e >= 2 ? 8 : 0);
-          const int hh = q * HS + nt * 8 + 2 * t4 + (e & 1);
-          *reinterpret_cast<bf16*>(sm + P.ea + swz(m, hh, MT)) =
-              __float2bfloat16_rn(silu(ag[i][e]) * au[i][e]);
+          const int hh = nt * 8 + 2 * t4 + (e & 1);
+          split_store(sm + P.ahi, sm + P.alo, swz(m, hh, MT), silu(ag[i][e]) * au[i][e]);
         }
     }
-    cluster.sync();
-    gather_peers<MTILES, 11>(cluster, sm + P.ea, HS, q);
     __syncthreads();
 
-    // ---- phase 3: lat (own channels) = u + a . w_down^T, K split over warp groups ----
-    if (warp < P.nt1 * P.ks1) {
-      const int nt = warp % P.nt1, ks = warp / P.nt1;
-      const int kl = H / P.ks1;
+    // ---- partial down projection over own units, every channel: P = a . w_down[:, own]^T ----
+    for (int nt = warp; nt < r / 8; nt += NW) {
       float acc[MTILES][4] = {};
-      warp_gemm<MTILES>(acc, aEA, aWd, CS, nt * 8, ks * kl, (ks + 1) * kl);
-      float* dst = sPart + ks * MT * ldp;
+      warp_gemm<MTILES>(acc, aAhi, aWdk, r, nt * 8, 0, HS);
+      warp_gemm<MTILES>(acc, aAlo, aWdk, r, nt * 8, 0, HS);
 #pragma unroll
       for (int i = 0; i < MTILES; ++i)
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-          dst[(i * 16 + g8 + (e >= 2 ? 8 : 0)) * ldp + nt * 8 + 2 * t4 + (e & 1)] = acc[i][e];
+          sP[(i * 16 + g8 + (e >= 2 ? 8 : 0)) * P.pp + nt * 8 + 2 * t4 + (e & 1)] = acc[i][e];
     }
-    __syncthreads();
+    cluster.sync();
+
+    // ---- lat (own channels) = u + sum_p P_p, p = 0..7 in order, over DSMEM ----
 #pragma unroll
     for (int k = 0; k < MAXU; ++k) {
       const int i = tid + k * THREADS;
       if (i < MT * CS) {
         const int m = i / CS, c = i % CS;
+        const int off = m * P.pp + q * CS + c;
+        float pv[CL];
+#pragma unroll
+        for (int p = 0; p < CL; ++p) pv[p] = *(cluster.map_shared_rank(sP, p) + off);
         if (m < rows && (m % B) != 0) {
           float v = sUs[m * ldp + c];
-          for (int ks = 0; ks < P.ks1; ++ks) v += sPart[ks * MT * ldp + m * ldp + c];
+#pragma unroll
+          for (int p = 0; p < CL; ++p) v += pv[p];
           const int n = n0 + m / B, b = m % B;
           lat[((int64_t)n * (B - 1) + b - 1) * r + q * CS + c] = __float2bfloat16_rn(v);
         }
       }
     }
-    cluster.sync();   // peers may still read this CTA's u / activation slices
+    cluster.sync();   // peers may still read this CTA's u halves and partial sums
   }
   // nothing may land in shared memory after the CTA exits
   if (tid == 0 && s_abort) {
@@ -386,52 +412,32 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1) latent_
   }
 }
 
-int g_max_clusters[2] = {0, 0};   // co-resident clusters per variant (queried once)
+int g_max_clusters = 0;   // co-resident clusters (queried once)
 
-template <int MTILES>
+size_t smem_bytes(int r, int H, int B) { return (size_t)make_plan(r, H, B).total + 1024; }
+
 int max_clusters(int smem) {
-  int& cached = g_max_clusters[MTILES - 2];
-  if (cached > 0) return cached;
+  if (g_max_clusters > 0) return g_max_clusters;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(CL);
   cfg.blockDim = dim3(THREADS);
   cfg.dynamicSmemBytes = smem;
   int n = 0;
-  if (cudaFuncSetAttribute(latent_mma_kernel<MTILES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           smem) != cudaSuccess ||
-      cudaOccupancyMaxActiveClusters(&n, latent_mma_kernel<MTILES>, &cfg) != cudaSuccess || n <= 0)
+  if (cudaFuncSetAttribute(latent_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+          cudaSuccess ||
+      cudaOccupancyMaxActiveClusters(&n, latent_mma_kernel, &cfg) != cudaSuccess || n <= 0)
     n = 1;
-  cached = n;
+  g_max_clusters = n;
   return n;
-}
-
-size_t smem_bytes(int MT, int r, int H, int B) { return (size_t)make_plan(MT, r, H, B).total + 1024; }
-
-template <int MTILES>
-cudaError_t launch(const xp_head* h, const int64_t* blk, const int64_t* am1, const float* xh,
-                   int N, void* lat, cudaStream_t s) {
-  const Plan P = make_plan(MTILES * 16, h->r, h->H, h->B);
-  const int smem = (int)smem_bytes(P.MT, h->r, h->H, h->B);
-  cudaError_t e = cudaFuncSetAttribute(latent_mma_kernel<MTILES>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
-  const int nb = P.MT / h->B;
-  const int groups = (N + nb - 1) / nb;
-  const int clusters = std::min(groups, max_clusters<MTILES>(smem));
-  const Maps maps = {h->tm_wlat, h->tm_wg, h->tm_wu, h->tm_wd, h->tm_mixT};
-  e = xp_launch_pdl(latent_mma_kernel<MTILES>, dim3(clusters * CL), dim3(THREADS), (size_t)smem,
-                    s, maps, blk, am1, xh, (const bf16*)h->w1, (bf16*)lat, N, h->B, h->r, h->H,
-                    h->V, h->err);
-  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace
 
 bool xp_latent_mma_ok(int r, int H, int B, xp_dtype dt) {
-  if (dt != XP_BF16 || B < 2 || B > 32) return false;
+  if (dt != XP_BF16 || B < 2 || B > MT) return false;
   if (r != 64 && r != 128 && r != 256) return false;      // r/8 channels = 1, 2 or 4 n-tiles
-  if (H % (8 * CL) != 0 || H > 1024) return false;
-  return smem_bytes(48, r, H, B) <= 227 * 1024;
+  if (H % (8 * 64) != 0 || H > 1024) return false;        // own units in 64-wide chunks
+  return smem_bytes(r, H, B) <= 227 * 1024;
 }
 
 // Tensor maps of the weight and mixer slices (2-D, bf16; weights 128B-swizzled).
@@ -454,15 +460,22 @@ bool xp_latent_mma_maps(xp_head* h) {
   return enc(&h->tm_wlat, h->w_lat, r, r, 64, CS, true) &&
          enc(&h->tm_wg, h->w_gate, H, r, 64, HS, true) &&
          enc(&h->tm_wu, h->w_up, H, r, 64, HS, true) &&
-         enc(&h->tm_wd, h->w_down, r, H, 64, CS, true) &&
+         enc(&h->tm_wd, h->w_down, r, H, 64, std::min(r, 256), true) &&
          enc(&h->tm_mixT, h->mixT, B * B, r, CS, std::min(B * B, 256), false);
 }
 
 cudaError_t xp_launch_latent_mma(const xp_head* h, const int64_t* blk, const int64_t* am1,
                                  const float* xh, int N, void* lat, cudaStream_t s) {
-  // 32-row groups while they fit in one wave of co-resident clusters, else 48-row groups
-  const int groups32 = (N + 32 / h->B - 1) / (32 / h->B);
-  if (groups32 <= max_clusters<2>((int)smem_bytes(32, h->r, h->H, h->B)))
-    return launch<2>(h, blk, am1, xh, N, lat, s);
-  return launch<3>(h, blk, am1, xh, N, lat, s);
+  const int smem = (int)smem_bytes(h->r, h->H, h->B);
+  cudaError_t e =
+      cudaFuncSetAttribute(latent_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const int nb = MT / h->B;
+  const int groups = (N + nb - 1) / nb;
+  const int clusters = std::min(groups, max_clusters(smem));
+  const Maps maps = {h->tm_wlat, h->tm_wg, h->tm_wu, h->tm_wd, h->tm_mixT};
+  e = xp_launch_pdl(latent_mma_kernel, dim3(clusters * CL), dim3(THREADS), (size_t)smem, s, maps,
+                    blk, am1, xh, (const bf16*)h->w1, (bf16*)lat, N, h->B, h->r, h->H, h->V,
+                    h->err);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
