@@ -193,7 +193,8 @@ def run_native(args, rank, world, local):
 
     passes = wl.K * args.steps * world
     value = passes / (ms / 1e3)
-    launches_per_step = 5 + 1 + 2 * wl.K if wl.topc == 0 else 5 + 2 + 2 * wl.K
+    # hidden cache (3 kernels) + init (1) or top-C select and gather (2) + 2 per pass
+    launches_per_step = 3 + 1 + 2 * wl.K if wl.topc == 0 else 3 + 2 + 2 * wl.K
     out = {
         "metric": "Jacobi passes/s at N=32,B=16,V=151936 bf16; % of HBM roofline",
         "value": round(value, 2), "unit": "passes/s", "n_gpus": world, "steps": args.steps,
