@@ -197,6 +197,17 @@ __global__ void hc_reduce_kernel(const float* __restrict__ G, int64_t split_stri
 
 }  // namespace
 
+cudaError_t xp_launch_embed_table(const xp_head* h, cudaStream_t s) {
+  const int smem = (int)(sizeof(bf16) * GB_STAGES * (GB_M + GB_N) * GB_PITCH);
+  cudaError_t e =
+      cudaFuncSetAttribute(gemm_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid((h->r + GB_N - 1) / GB_N, (h->V + GB_M - 1) / GB_M, 1);
+  gemm_bf16_kernel<<<grid, 256, smem, s>>>((const bf16*)h->w1, h->r, (const bf16*)h->w_lat, h->r,
+                                           h->E, h->r, 0, h->V, h->r, h->r);
+  return cudaGetLastError();
+}
+
 int xp_hidden_splits(int rows, int r, int hidden, int num_sms, int cap_rows) {
   const int tiles = ((rows + GB_M - 1) / GB_M) * ((2 * r + GB_N - 1) / GB_N);
   int splits = std::max(1, (2 * num_sms + tiles - 1) / tiles);

@@ -28,7 +28,7 @@ bool valid_weight_ptrs(const xp_weights* w) {
 }
 
 struct PrepLayout {
-  size_t err, w1, down_hg, w_hc, w_lat, mix, mixT, w_gate, w_up, w_down, w2, total;
+  size_t err, w1, down_hg, w_hc, w_lat, mix, mixT, w_gate, w_up, w_down, w2, E, total;
 };
 
 PrepLayout prep_layout(const xp_weights* w) {
@@ -48,6 +48,8 @@ PrepLayout prep_layout(const xp_weights* w) {
   L.w_up = take(H * r * es);
   L.w_down = take(r * H * es);
   L.w2 = take(V * r * es);
+  // projected embedding table, only where the tensor-core latent runs
+  L.E = take(xp_latent_mma_ok(w->r, w->H, w->B, w->dtype) ? V * r * 4 : 0);
   L.total = o;
   return L;
 }
@@ -75,6 +77,7 @@ xp_status copy_weights(xp_head* h, const xp_weights* w, cudaStream_t s) {
   cp(h->w_up, w->w_up, H * r * es);
   cp(h->w_down, w->w_down, r * H * es);
   cp(h->w2, w->w2, V * r * es);
+  if (e == cudaSuccess && h->latent_mma) e = xp_launch_embed_table(h, s);
   return e == cudaSuccess ? XP_OK : XP_ECUDA;
 }
 
@@ -173,11 +176,12 @@ xp_status xp_head_create(const xp_weights* w, void* prep_dev, size_t prep_bytes,
   h->w1 = p + L.w1; h->down_hg = p + L.down_hg;
   h->w_hc = p + L.w_hc; h->w_lat = p + L.w_lat; h->mix = p + L.mix;
   h->mixT = p + L.mixT;
+  h->E = (float*)(p + L.E);
   h->w_gate = p + L.w_gate; h->w_up = p + L.w_up; h->w_down = p + L.w_down; h->w2 = p + L.w2;
+  decide_paths(h);
   xp_status st = copy_weights(h, w, stream);
   if (st == XP_OK) st = cuda_status(cudaMemsetAsync(h->err, 0, 256, stream));
   if (st != XP_OK) { delete h; return st; }
-  decide_paths(h);
   *out = h;
   return XP_OK;
 }

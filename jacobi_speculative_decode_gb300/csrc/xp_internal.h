@@ -18,10 +18,11 @@ struct xp_head {
   uint32_t* err;         // device error word (XP_ERR_* bits)
   void *w1, *down_hg, *w_hc, *w_lat, *mix, *w_gate, *w_up, *w_down, *w2;  // down_hg = [down_h ; down_g]
   void* mixT;            // folded mixer laid out [out slot][in slot][channel]
+  float* E;              // w1 . in_proj[:, 2r:]^T, fp32 [V, r] (tensor-core latent only)
   int readout_tc;        // tcgen05 readout usable for this head's shapes
   int latent_mma;        // cluster tensor-core latent usable for this head's shapes
   CUtensorMap tm_w2;     // W2 [V, r] tiled map for the tcgen05 readout
-  CUtensorMap tm_wlat, tm_wg, tm_wu, tm_wd, tm_mixT;   // latent weight slices (TMA)
+  CUtensorMap tm_wg, tm_wu, tm_wd, tm_mixT;   // latent weight / mixer slices (TMA)
 };
 
 // device error word bits
@@ -46,6 +47,9 @@ static inline size_t xp_elem(xp_dtype d) { return d == XP_BF16 ? 2 : 4; }
 cudaError_t xp_launch_fold(const void* raw, void* mix, int r, int B, xp_dtype dt, cudaStream_t s);
 cudaError_t xp_launch_mix_transpose(const void* mix, void* mixT, int r, int B, xp_dtype dt,
                                     cudaStream_t s);
+
+// E = w1 . w_lat^T, the projected embedding table of the tensor-core latent
+cudaError_t xp_launch_embed_table(const xp_head* h, cudaStream_t s);
 
 cudaError_t xp_launch_hidden(const xp_head* h, const void* h_full, int N, float* xh, float* part,
                              float* hc, int part_rows, cudaStream_t s);
