@@ -15,10 +15,11 @@
 //   2. u = per-channel causal mix of x (fp32); push the own u slice to every CTA
 //      of the cluster as a bf16 hi + lo pair (u = hi + lo to ~2^-17) with
 //      st.async, which completes bytes on the receiver's mbarrier
-//   3. a = silu(u w_gate[own]^T) * (u w_up[own]^T) from hi and lo (mma.sync)
-//   4. partial = a w_down[:, own]^T for ALL channels (w_down's column slice
-//      arrives by TMA into the u buffer, dead by then); each 8-channel piece is
-//      pushed to the CTA owning those channels
+//   3. a = silu(u w_gate[own]^T) * (u w_up[own]^T) from hi and lo: tcgen05.mma
+//      (M = 128 rows, of which the group's MT are real) into TMEM, kept as hi + lo
+//   4. partial = a w_down[:, own]^T for ALL channels, tcgen05.mma again (w_down's
+//      column slice arrives by TMA into the u buffer, dead by then); each
+//      32-channel piece is pushed to the CTA owning those channels
 //   5. lat = u + the 8 partials of the own channels, added in a fixed order
 // The only cluster-wide barrier per group is a split arrive/wait that keeps a
 // CTA from pushing into buffers a peer is still reading.
@@ -41,7 +42,6 @@ namespace {
 
 constexpr int CL = 8;          // CTAs per cluster
 constexpr int THREADS = 256;   // 8 warps
-constexpr int NW = THREADS / 32;
 
 struct Plan {                  // byte offsets into dynamic shared memory
   int MT, CS, HS;
@@ -91,24 +91,6 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-__device__ __forceinline__ void ldm_x4(uint32_t (&r)[4], uint32_t addr) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-__device__ __forceinline__ void ldm_x2(uint32_t (&r)[2], uint32_t addr) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];"
-               : "=r"(r[0]), "=r"(r[1])
-               : "r"(addr));
-}
-__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4],
-                                         const uint32_t (&b)[2]) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
-      "{%8, %9}, {%0, %1, %2, %3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
-}
 
 // ---- cluster (distributed shared memory) helpers ----
 __device__ __forceinline__ uint32_t mapa(uint32_t local, int rank) {
@@ -122,12 +104,6 @@ __device__ __forceinline__ void st_async16(uint32_t raddr, uint4 v, uint32_t rba
       "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
           raddr),
       "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(rbar)
-      : "memory");
-}
-__device__ __forceinline__ void st_async8(uint32_t raddr, float a, float b, uint32_t rbar) {
-  asm volatile(
-      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.b32 [%0], {%1, %2}, [%3];" ::"r"(raddr),
-      "r"(__float_as_uint(a)), "r"(__float_as_uint(b)), "r"(rbar)
       : "memory");
 }
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
@@ -168,6 +144,9 @@ struct Maps {
   CUtensorMap wg, wu, wdk, mix;
 };
 
+constexpr uint32_t TMEM_COLS = 512;    // gate 64 | up 64 | partial sums 256 (r <= 256)
+constexpr uint32_t COL_G = 0, COL_U = 64, COL_P = 128;
+
 template <int MTILES>
 __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1) latent_mma_kernel(
     const __grid_constant__ Maps maps, const int64_t* __restrict__ blk,
@@ -191,8 +170,9 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1) latent_
   float* sUs = (float*)(sm + P.us);
   int64_t* sPrev = (int64_t*)(sm + P.prev);
   const uint32_t bar_w = s0 + P.bars, bar_wd = bar_w + 8, bar_u = bar_w + 16, bar_p = bar_w + 24;
+  const uint32_t bar_mma = bar_w + 32;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + P.bars + 40);
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-  const int g8 = lane / 4, t4 = lane % 4;
   const int nb = MT / B;                   // blocks per group
   const int groups = (N + nb - 1) / nb;
   const int ldp = CS + 1;
@@ -206,6 +186,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1) latent_
     ptx::mbar_init(bar_wd, 1);
     ptx::mbar_init(bar_u, 1);
     ptx::mbar_init(bar_p, 1);
+    ptx::mbar_init(bar_mma, 1);
     ptx::fence_barrier_init();
     const int mparts = (P.mix_rows + 255) / 256, mbox = std::min(P.mix_rows, 256);
     ptx::mbar_arrive_expect_tx(bar_w, 2 * HS * r * 2 + mparts * mbox * CS * 2);
@@ -219,15 +200,27 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1) latent_
     ptx::mbar_arrive_expect_tx(bar_u, u_bytes_in);
     ptx::mbar_arrive_expect_tx(bar_p, p_bytes_in);
   }
+  if (warp == 0) {
+    ptx::tmem_alloc(ptx::smem_u32(s_tmem), TMEM_COLS);
+    ptx::tmem_relinquish();
+  }
   // peers push into this CTA only after its barriers exist
+  ptx::tc_fence_before();
   cluster_arrive();
   ptx::pdl_wait();                         // blk (and xh) come from earlier kernels
   ptx::pdl_trigger();
   cluster_wait();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *s_tmem;
   {
     volatile int no_abort = 0;
     ptx::mbar_wait(bar_w, 0, &no_abort, err);
   }
+  uint32_t mma_phase = 0;
+  // TMEM readers: warps whose lane quadrant holds real rows (MT <= 64), two column halves
+  const bool reader = (warp & 3) * 32 < MT;
+  const int quad = warp & 3, half = warp >> 2;
+  const int trow = quad * 32 + lane;        // this thread's row when it is a reader
 
   int it = 0;
   for (int grp = cid; grp < groups; grp += nclusters, ++it) {
@@ -323,41 +316,62 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1) latent_
     __syncthreads();
     mbar_wait_cluster(bar_u, ph, err);
 
-    // ---- 3. SwiGLU on own hidden units from u = hi + lo ----
-    for (int nt = warp; nt < HS / 8; nt += NW) {
-      float g0[MTILES][4] = {}, g1[MTILES][4] = {}, v0[MTILES][4] = {}, v1[MTILES][4] = {};
-      const int ar = lane % 16, ak = (lane / 16) * 8;
-      const int br = nt * 8 + (lane % 8), bk = ((lane / 8) % 2) * 8;
-      for (int k = 0; k < r; k += 16) {
-        uint32_t bg[2], bu[2];
-        const int bo = swz(br, k + bk, HS);
-        ldm_x2(bg, aWg + bo);
-        ldm_x2(bu, aWu + bo);
+    // ---- 3. SwiGLU on own hidden units from u = hi + lo (tcgen05, fp32 in TMEM) ----
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // u seen by the MMA
+    __syncthreads();
+    if (tid == 0) {
+      ptx::tc_fence_after();
+      constexpr uint32_t ID64 = ptx::idesc_bf16_f32(128, 64);
+      int first = 1;
+      for (int kc = 0; kc < r / 64; ++kc)
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint32_t ko = kc * MT * 128 + kk * 32;
+          const uint64_t bg = ptx::sw128_desc(aWg + kc * HS * 128 + kk * 32);
+          const uint64_t bu = ptx::sw128_desc(aWu + kc * HS * 128 + kk * 32);
+          const uint64_t ah = ptx::sw128_desc(aUhi + ko), al = ptx::sw128_desc(aUlo + ko);
+          ptx::mma_bf16(tmem + COL_G, ah, bg, ID64, !first);
+          ptx::mma_bf16(tmem + COL_U, ah, bu, ID64, !first);
+          ptx::mma_bf16(tmem + COL_G, al, bg, ID64, 1);
+          ptx::mma_bf16(tmem + COL_U, al, bu, ID64, 1);
+          first = 0;
+        }
+      ptx::mma_commit(bar_mma);
+    }
+    {
+      volatile int no_abort = 0;
+      ptx::mbar_wait(bar_mma, mma_phase, &no_abort, err);
+      mma_phase ^= 1;
+    }
+    ptx::tc_fence_after();
+    if (reader) {
+      // each reader thread: its row, 32 of the 64 own hidden units (gate and up)
+      uint32_t g[32], v[32];
+      const uint32_t ta = tmem + ((uint32_t)(quad * 32) << 16) + half * 32;
+      ptx::tmem_ld32(ta + COL_G, g);
+      ptx::tmem_ld32(ta + COL_U, v);
+      ptx::tmem_wait_ld();
+      if (trow < MT) {
 #pragma unroll
-        for (int i = 0; i < MTILES; ++i) {
-          uint32_t ah[4], al[4];
-          const int ao = swz(i * 16 + ar, k + ak, MT);
-          ldm_x4(ah, aUhi + ao);
-          ldm_x4(al, aUlo + ao);
-          mma16816(g0[i], ah, bg);
-          mma16816(v0[i], ah, bu);
-          mma16816(g1[i], al, bg);
-          mma16816(v1[i], al, bu);
+        for (int c8 = 0; c8 < 4; ++c8) {
+          uint32_t hw[4], lw[4];
+#pragma unroll
+          for (int e = 0; e < 8; e += 2) {
+            const int k = c8 * 8 + e;
+            const float a0 = silu(__uint_as_float(g[k])) * __uint_as_float(v[k]);
+            const float a1 = silu(__uint_as_float(g[k + 1])) * __uint_as_float(v[k + 1]);
+            const __nv_bfloat162 h2 = __floats2bfloat162_rn(a0, a1);
+            const float2 hf = __bfloat1622float2(h2);
+            const __nv_bfloat162 l2 = __floats2bfloat162_rn(a0 - hf.x, a1 - hf.y);
+            hw[e / 2] = *reinterpret_cast<const uint32_t*>(&h2);
+            lw[e / 2] = *reinterpret_cast<const uint32_t*>(&l2);
+          }
+          const int off = swz(trow, half * 32 + c8 * 8, MT);
+          *reinterpret_cast<uint4*>(sm + P.ahi + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+          *reinterpret_cast<uint4*>(sm + P.alo + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
         }
       }
-#pragma unroll
-      for (int i = 0; i < MTILES; ++i)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int m = i * 16 + g8 + (e >= 2 ? 8 : 0);
-          const int hh = nt * 8 + 2 * t4 + (e & 1);
-          const float a = silu(g0[i][e] + g1[i][e]) * (v0[i][e] + v1[i][e]);
-          const bf16 ah = __float2bfloat16_rn(a);
-          const int off = swz(m, hh, MT);
-          *reinterpret_cast<bf16*>(sm + P.ahi + off) = ah;
-          *reinterpret_cast<bf16*>(sm + P.alo + off) = __float2bfloat16_rn(a - __bfloat162float(ah));
-        }
     }
+    ptx::tc_fence_before();
     __syncthreads();                         // u is dead: w_down's slice may overwrite it
     if (tid == 0) {
       ptx::mbar_arrive_expect_tx(bar_wd, r * HS * 2);
@@ -372,41 +386,51 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1) latent_
       ptx::mbar_wait(bar_wd, ph, &no_abort, err);
     }
 
-    // ---- 4. partial down projection over own units, pushed to each channel's owner ----
-    for (int nt = warp; nt < r / 8; nt += NW) {
-      float c0[MTILES][4] = {}, c1[MTILES][4] = {};
-      const int ar = lane % 16, ak = (lane / 16) * 8;
-      const int br = nt * 8 + (lane % 8), bk = ((lane / 8) % 2) * 8;
-      for (int k = 0; k < HS; k += 16) {
-        uint32_t bw[2];
-        ldm_x2(bw, aU + swz(br, k + bk, r));
+    // ---- 4. partial down projection over own units (tcgen05), pushed to each owner ----
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // activations seen by the MMA
+    __syncthreads();
+    if (tid == 0) {
+      ptx::tc_fence_after();
+      const uint32_t idn = ptx::idesc_bf16_f32(128, r);
+      for (int kc = 0; kc < HS / 64; ++kc)
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint64_t bw = ptx::sw128_desc(aU + kc * r * 128 + kk * 32);
+          const uint32_t ko = kc * MT * 128 + kk * 32;
+          ptx::mma_bf16(tmem + COL_P, ptx::sw128_desc(aAhi + ko), bw, idn, (kc | kk) != 0);
+          ptx::mma_bf16(tmem + COL_P, ptx::sw128_desc(aAlo + ko), bw, idn, 1);
+        }
+      ptx::mma_commit(bar_mma);
+    }
+    {
+      volatile int no_abort = 0;
+      ptx::mbar_wait(bar_mma, mma_phase, &no_abort, err);
+      mma_phase ^= 1;
+    }
+    ptx::tc_fence_after();
+    if (reader) {
+      // each reader thread: its row, channels [half*r/2, (half+1)*r/2), 32 at a time
+      const uint32_t ta = tmem + ((uint32_t)(quad * 32) << 16) + COL_P;
+      for (int c32 = half * (r / 64); c32 < (half + 1) * (r / 64); ++c32) {
+        uint32_t pv[32];
+        ptx::tmem_ld32(ta + c32 * 32, pv);
+        ptx::tmem_wait_ld();
+        if (trow < MT) {
+          // channels [c32*32, c32*32+32) belong to owner c32*32 / CS
 #pragma unroll
-        for (int i = 0; i < MTILES; ++i) {
-          uint32_t ah[4], al[4];
-          const int ao = swz(i * 16 + ar, k + ak, MT);
-          ldm_x4(ah, aAhi + ao);
-          ldm_x4(al, aAlo + ao);
-          mma16816(c0[i], ah, bw);
-          mma16816(c1[i], al, bw);
+          for (int c4 = 0; c4 < 8; ++c4) {
+            const int c = c32 * 32 + c4 * 4;
+            const int owner = c / CS, cl = c - owner * CS;
+            const uint32_t o = s0 + P.rcv + (uint32_t)(((q * MT + trow) * CS + cl) * 4);
+            const uint4 v4 = make_uint4(pv[c4 * 4], pv[c4 * 4 + 1], pv[c4 * 4 + 2], pv[c4 * 4 + 3]);
+            if (owner == q)
+              *reinterpret_cast<uint4*>(sm + (o - s0)) = v4;
+            else
+              st_async16(mapa(o, owner), v4, mapa(bar_p, owner));
+          }
         }
       }
-      const int owner = nt * 8 / CS, cl0 = nt * 8 - owner * CS;
-      const uint32_t slot = s0 + P.rcv + (uint32_t)(q * MT * CS * 4);   // my slot at the owner
-      const uint32_t rb = mapa(bar_p, owner);
-#pragma unroll
-      for (int i = 0; i < MTILES; ++i)
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const int m = i * 16 + g8 + hh * 8;
-          const float a = c0[i][2 * hh] + c1[i][2 * hh];
-          const float b = c0[i][2 * hh + 1] + c1[i][2 * hh + 1];
-          const uint32_t o = slot + (uint32_t)((m * CS + cl0 + 2 * t4) * 4);
-          if (owner == q)
-            *reinterpret_cast<float2*>(sm + (o - s0)) = make_float2(a, b);
-          else
-            st_async8(mapa(o, owner), a, b, rb);
-        }
     }
+    ptx::tc_fence_before();
     __syncthreads();
     mbar_wait_cluster(bar_p, ph, err);
 
@@ -431,6 +455,10 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1) latent_
     cluster_arrive();
   }
   cluster_wait();   // no CTA leaves while a peer may still push into it
+  if (warp == 0) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, TMEM_COLS);
+  }
 }
 
 int g_max_clusters[2] = {0, 0};   // co-resident clusters per variant (queried once)
@@ -479,7 +507,7 @@ cudaError_t launch(const xp_head* h, const int64_t* blk, const int64_t* am1, con
 bool xp_latent_mma_ok(int r, int H, int B, xp_dtype dt) {
   if (dt != XP_BF16 || B < 2 || B > 32) return false;
   if (r != 64 && r != 128 && r != 256) return false;      // r/8 channels: 8, 16 or 32
-  if (H % (8 * 64) != 0 || H > 1024) return false;        // own units in 64-wide chunks
+  if (H != 8 * 64) return false;                          // 64 own units: one MMA N-tile
   return smem_bytes(48, r, H, B) <= 227 * 1024;
 }
 
