@@ -172,6 +172,29 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
   return d;
 }
 
+// Same for 64-byte swizzling: rows of 32 bf16 (64 B), 8-row groups 512 B apart.
+__device__ __forceinline__ uint64_t sw64_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;
+  d |= (uint64_t)(512 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)4 << 61;                          // swizzle mode: 64 B
+  return d;
+}
+
+// Bulk copy of `bytes` (multiple of 16) from this CTA's shared memory into a
+// cluster peer's (dst and mbar are shared::cluster addresses of that peer);
+// the bytes complete on the peer's mbarrier.
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst, uint32_t src, uint32_t bytes,
+                                                  uint32_t mbar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "r"(src), "r"(bytes), "r"(mbar)
+      : "memory");
+}
+
 // Instruction descriptor, kind::f16: bf16 A and B (both K-major), fp32 D, M x N.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
   return (1u << 4)                       // D format: f32
