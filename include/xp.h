@@ -140,6 +140,22 @@ xp_status xp_readout_argmax(const xp_head* head, const void* lat, const void* ba
                             int64_t stride_n, int64_t stride_b, int N, int64_t* blk,
                             float* win_val, void* ws, cudaStream_t stream);
 
+/* xp_readout_argmax for callers that cannot allocate device memory -- no
+ * counterpart on the pages; the refinement method itself says nothing about
+ * where scratch lives.  Same arguments and results as xp_readout_argmax,
+ * without the workspace: the cross-CTA argmax scratch (48 KB) is a fixed array
+ * in the library's device memory, present on every GPU that loads the library
+ * until the process exits.  Meant for callers that run inside a memory pool
+ * they do not own, or on a path where cudaMalloc and the synchronisation it can
+ * bring are not acceptable.  Limit: N*(B-1) <= 4096 draft rows, else
+ * XP_ECAPACITY.  The first call on a device looks the array up (once per
+ * device, on the current device); make that first call before any stream
+ * capture.  All calls share the one array, so calls that overlap on the GPU
+ * (other streams, other threads) race; each call clears it before use. */
+xp_status xp_readout_argmax_noalloc(const xp_head* head, const void* lat, const void* base,
+                                    int64_t stride_n, int64_t stride_b, int N, int64_t* blk,
+                                    float* win_val, cudaStream_t stream);
+
 /* Initial block: blk[n,0] = anchor[n], blk[n,1+b] = argmax_v base[n,b,v].
  * Same base addressing as xp_readout_argmax.  anchor: device [N] int64.
  * qwen3_xpress page, jacobi_refine_greedy (before the passes). */

@@ -53,6 +53,7 @@ _SIGS = {
     "xp_hidden_cache": (_I, [_P, _P, _I, _P, _P, _P]),
     "xp_latent_pass": (_I, [_P, _P, _P, _P, _I, _P, _P]),
     "xp_readout_argmax": (_I, [_P, _P, _P, _I64, _I64, _I, _P, _P, _P, _P]),
+    "xp_readout_argmax_noalloc": (_I, [_P, _P, _P, _I64, _I64, _I, _P, _P, _P]),
     "xp_init_argmax": (_I, [_P, _P, _I64, _I64, _P, _I, _P, _P, _P, _P]),
     "xp_topc_gather": (_I, [_P, _P, _I64, _I64, _I, _I, _P, _P, _P, _P, _P]),
     "xp_topc_readout_argmax": (_I, [_P, _P, _P, _P, _P, _I, _I, _P, _P, _P]),
@@ -170,6 +171,13 @@ def xp_latent_pass(head, blk, am1, xh, N, lat, stream=None):
 def xp_readout_argmax(head, lat, base, stride_n, stride_b, N, blk, win_val, ws, stream=None):
     _check("xp_readout_argmax", lib().xp_readout_argmax(
         head, _ptr(lat), _ptr(base), stride_n, stride_b, N, _ptr(blk), _ptr(win_val), _ptr(ws),
+        _stream(stream)))
+
+
+def xp_readout_argmax_noalloc(head, lat, base, stride_n, stride_b, N, blk, win_val, stream=None):
+    """xp_readout_argmax without a workspace, for callers that cannot allocate device memory."""
+    _check("xp_readout_argmax_noalloc", lib().xp_readout_argmax_noalloc(
+        head, _ptr(lat), _ptr(base), stride_n, stride_b, N, _ptr(blk), _ptr(win_val),
         _stream(stream)))
 
 
