@@ -42,6 +42,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-breakdown", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the single-request, top-C and max-batch side measurements")
     return ap.parse_args()
 
 
@@ -221,7 +223,87 @@ def run_native(args, rank, world, local):
     if rank == 0 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(wl, d, budget_s=12.0)
     head.close()
+    del d, base, h, ws
+    if rank == 0 and world == 1 and not args.no_extras:
+        out["other_workloads"] = other_workloads(args)
     return out
+
+
+def other_workloads(args):
+    """Side measurements on the other workloads (not the headline): passes/s of a full
+    step, and for top-C the per-pass candidate readout against the HBM roofline."""
+    import torch
+    from jacobi_speculative_decode_gb300 import inputs as I
+    from jacobi_speculative_decode_gb300 import xp
+    res = {}
+    hbm, kind = peaks()
+    for name in ("single-request", "topc", "max-batch"):
+        wl = I.workload(name)
+        d = I.make_inputs(wl)
+        head, _ = xp.head_from_inputs(d, wl)
+        base = xp.to_device(d["base"], wl.dtype)
+        h = xp.to_device(d["h_full"], wl.dtype)
+        anchor = torch.from_numpy(d["anchor"]).cuda()
+        am1 = torch.from_numpy(d["am1"]).cuda()
+        blk = torch.empty(wl.N, wl.B, dtype=torch.int64, device="cuda")
+        ws = head.workspace(wl.N, wl.topc)
+        sn, sb = (wl.B - 1) * wl.V, wl.V
+        stream = torch.cuda.current_stream()
+
+        def step():
+            xp.xp_jacobi_refine(head.handle, base, sn, sb, h, anchor, am1, wl.N, wl.K, wl.topc,
+                                blk, ws)
+
+        for _ in range(2):
+            step()
+        steps = 5
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / steps
+        r = {"passes_per_s": round(wl.K / (ms / 1e3), 1), "ms_per_step": round(ms, 4),
+             "rows_per_s": round(wl.K * wl.rows / (ms / 1e3), 1),
+             "config": {"N": wl.N, "B": wl.B, "V": wl.V, "hidden": wl.hidden, "K": wl.K,
+                        "topc": wl.topc}}
+        if xp.xp_get_error(head.handle) != xp.XP_OK:
+            r["device_error"] = True
+        if wl.topc:
+            C = wl.topc
+            cand = torch.empty(wl.N, wl.B - 1, C, dtype=torch.int64, device="cuda")
+            base_c = torch.empty(wl.N, wl.B - 1, C, dtype=torch.bfloat16, device="cuda")
+            w2c = torch.empty(wl.N, wl.B - 1, C, wl.r, dtype=torch.bfloat16, device="cuda")
+            lat = torch.empty(wl.N, wl.B - 1, wl.r, dtype=torch.bfloat16, device="cuda")
+            g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            g0.record(stream)
+            xp.xp_topc_gather(head.handle, base, sn, sb, wl.N, C, cand, base_c, w2c, blk)
+            g1.record(stream)
+            lat.copy_(torch.randn_like(lat, dtype=torch.float32).to(torch.bfloat16))
+            for _ in range(3):
+                xp.xp_topc_readout_argmax(head.handle, lat, base_c, cand, w2c, wl.N, C, blk, None)
+            n = 20
+            t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            t0.record(stream)
+            for _ in range(n):
+                xp.xp_topc_readout_argmax(head.handle, lat, base_c, cand, w2c, wl.N, C, blk, None)
+            t1.record(stream)
+            torch.cuda.synchronize()
+            us = t0.elapsed_time(t1) / n * 1e3
+            rows = wl.rows
+            nbytes = rows * C * wl.r * 2 + rows * C * 2 + rows * C * 8 + rows * wl.r * 2 + rows * 8
+            r["topc_readout"] = {"us": round(us, 2), "algorithmic_bytes": nbytes,
+                                 "achieved_gbs": round(nbytes / us / 1e3, 1),
+                                 "frac_of_hbm": round(nbytes / us / 1e3 / hbm, 4)}
+            r["topc_gather_us"] = round(g0.elapsed_time(g1) * 1e3, 1)
+            del cand, base_c, w2c, lat
+        res[name] = r
+        head.close()
+        del d, base, h, ws, blk
+        torch.cuda.empty_cache()
+    return res
 
 
 def breakdown(wl, head, base, sn, sb, h, anchor, am1, ws, stream, rank):
