@@ -1,5 +1,6 @@
-// Dense products of the hidden cache (once per draft step; qwen3_xpress page,
-// hidden_cache and the hoisted xh = hcache @ in_proj[:, :2r]^T):
+// Dense products of the hidden cache in unfolded form (once per draft step; qwen3_xpress
+// page, hidden_cache and the hoisted xh = hcache @ in_proj[:, :2r]^T), for the heads
+// and calls the folded tcgen05 path (k_hidden_tc.cu) does not take:
 //   G   = h . [down_h ; down_g]^T        [N*B, 2r]   bf16 tensor cores (split-K partials)
 //   hc  = [G_h ; mean over the block of G_g]            fp32  (mean commutes with down_g)
 //   xh  = hc . in_proj[:, :2r]^T          [N*B, r]    fp32 SIMT (hc is never rounded)
@@ -218,6 +219,10 @@ int xp_hidden_splits(int rows, int r, int hidden, int num_sms, int cap_rows) {
 
 cudaError_t xp_launch_hidden(const xp_head* h, const void* h_full, int N, float* xh, float* part,
                              float* hc, int part_rows, cudaStream_t s) {
+  if (xp_hidden_tc_call_ok(h, h_full)) {
+    const cudaError_t e = xp_launch_hidden_tc(h, h_full, N, xh, part, part_rows, s);
+    if (e != cudaErrorNotSupported) return e;
+  }
   const int B = h->B, r = h->r, hid = h->hidden, rows = N * B;
   const int64_t stride = (int64_t)rows * 2 * r;
   int splits = 1;

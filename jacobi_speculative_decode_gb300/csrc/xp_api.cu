@@ -28,7 +28,7 @@ bool valid_weight_ptrs(const xp_weights* w) {
 }
 
 struct PrepLayout {
-  size_t err, w1, down_hg, w_hc, w_lat, mix, mixT, w_gate, w_up, w_down, w2, E, total;
+  size_t err, w1, down_hg, w_hc, w_lat, mix, mixT, w_gate, w_up, w_down, w2, E, hfold, total;
 };
 
 PrepLayout prep_layout(const xp_weights* w) {
@@ -50,6 +50,8 @@ PrepLayout prep_layout(const xp_weights* w) {
   L.w2 = take(V * r * es);
   // projected embedding table, only where the tensor-core latent runs
   L.E = take(xp_latent_mma_ok(w->r, w->H, w->B, w->dtype) ? V * r * 4 : 0);
+  // folded hidden-cache projection (hi and lo bf16 planes), only where the tcgen05 path runs
+  L.hfold = take(xp_hidden_tc_ok(w->r, w->hidden, w->dtype) ? 2 * 2 * r * hid * 2 : 0);
   L.total = o;
   return L;
 }
@@ -78,6 +80,7 @@ xp_status copy_weights(xp_head* h, const xp_weights* w, cudaStream_t s) {
   cp(h->w_down, w->w_down, r * H * es);
   cp(h->w2, w->w2, V * r * es);
   if (e == cudaSuccess && h->latent_mma) e = xp_launch_embed_table(h, s);
+  if (e == cudaSuccess && h->hidden_tc) e = xp_launch_hidden_fold(h, w->in_proj, s);
   return e == cudaSuccess ? XP_OK : XP_ECUDA;
 }
 
@@ -105,7 +108,7 @@ xp_ws_layout xp_layout(int V, int hidden, int r, int B, int max_N, xp_dtype dt, 
   L.zero_end = o;
   L.xh = take((size_t)max_N * B * r * 4);
   L.lat = take(rows_cap * r * es);
-  L.part_rows = std::max(4096, max_N * B);
+  L.part_rows = std::max(8192, 2 * max_N * B);
   L.part = take((size_t)L.part_rows * 2 * r * 4);
   L.hc = take((size_t)max_N * B * 2 * r * 4);
   const size_t rows = (size_t)std::max(N, 0) * (B - 1);
@@ -177,6 +180,7 @@ xp_status xp_head_create(const xp_weights* w, void* prep_dev, size_t prep_bytes,
   h->w_hc = p + L.w_hc; h->w_lat = p + L.w_lat; h->mix = p + L.mix;
   h->mixT = p + L.mixT;
   h->E = (float*)(p + L.E);
+  h->hfold = p + L.hfold;
   h->w_gate = p + L.w_gate; h->w_up = p + L.w_up; h->w_down = p + L.w_down; h->w2 = p + L.w2;
   decide_paths(h);
   xp_status st = copy_weights(h, w, stream);
@@ -367,12 +371,14 @@ xp_encode_tiled_fn xp_get_encode_tiled() {
 static void decide_paths(xp_head* h) {
   h->readout_tc = 0;
   h->latent_mma = 0;
+  h->hidden_tc = 0;
   int major = 0, minor = 0;
   cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, h->device);
   cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, h->device);
   const bool blackwell = major == 10 && minor == 3;
   if (!blackwell || h->dtype != XP_BF16) return;
   h->latent_mma = xp_latent_mma_ok(h->r, h->H, h->B, h->dtype) && xp_latent_mma_maps(h);
+  h->hidden_tc = xp_hidden_tc_ok(h->r, h->hidden, h->dtype) && xp_hidden_tc_map(h);
   // tcgen05 readout: K = r tiled by 64-wide (128-byte) swizzled chunks, at most 4
   // of them resident; draft rows of one block never straddle a 128-row tile
   if (h->r % 64 == 0 && h->r <= 256 && h->B - 1 <= 128 && xp_get_encode_tiled()) {

@@ -19,6 +19,9 @@ struct xp_head {
   void *w1, *down_hg, *w_hc, *w_lat, *mix, *w_gate, *w_up, *w_down, *w2;  // down_hg = [down_h ; down_g]
   void* mixT;            // folded mixer laid out [out slot][in slot][channel]
   float* E;              // w1 . in_proj[:, 2r:]^T, fp32 [V, r] (tensor-core latent only)
+  void* hfold;           // [in_proj[:, :r] . down_h ; in_proj[:, r:2r] . down_g] as bf16 hi, lo planes
+  int hidden_tc;         // tcgen05 hidden cache usable for this head's shapes
+  CUtensorMap tm_hfold;  // hfold viewed as [4r, hidden] (hi rows, then lo rows)
   int readout_tc;        // tcgen05 readout usable for this head's shapes
   int latent_mma;        // cluster tensor-core latent usable for this head's shapes
   CUtensorMap tm_w2;     // W2 [V, r] tiled map for the tcgen05 readout
@@ -53,6 +56,14 @@ cudaError_t xp_launch_embed_table(const xp_head* h, cudaStream_t s);
 
 cudaError_t xp_launch_hidden(const xp_head* h, const void* h_full, int N, float* xh, float* part,
                              float* hc, int part_rows, cudaStream_t s);
+// tcgen05 hidden cache over the folded projection (bf16 heads, 2r a multiple of 256)
+bool xp_hidden_tc_ok(int r, int hidden, xp_dtype dt);
+bool xp_hidden_tc_map(xp_head* h);
+cudaError_t xp_launch_hidden_fold(const xp_head* h, const void* in_proj, cudaStream_t s);
+bool xp_hidden_tc_call_ok(const xp_head* h, const void* h_full);
+// returns cudaErrorNotSupported when h_full cannot be tiled by TMA
+cudaError_t xp_launch_hidden_tc(const xp_head* h, const void* h_full, int N, float* xh,
+                                float* part, int part_rows, cudaStream_t s);
 
 cudaError_t xp_launch_init_argmax(const xp_head* h, const void* base, int64_t sn, int64_t sb,
                                   const int64_t* anchor, int N, int64_t* blk, float* win,

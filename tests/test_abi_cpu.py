@@ -52,9 +52,10 @@ def test_sizes(lib):
     es = 2
     prep = xp.xp_head_prep_bytes(w)
     # every prepared copy is present: w1 + w2 + down_h + down_g + in_proj + mix + MLP,
-    # plus the [b][j][channel] copy of the mixer and the fp32 projected embedding table
+    # plus the [b][j][channel] copy of the mixer, the fp32 projected embedding table and
+    # the folded hidden-cache projection [2r, hidden] as two bf16 planes (hi, lo)
     floor = es * (2 * 151936 * 256 + 2 * 256 * 4096 + 3 * 256 * 256 + 256 * 16 * 16 + 3 * 512 * 256)
-    floor += es * 256 * 16 * 16 + 4 * 151936 * 256
+    floor += es * 256 * 16 * 16 + 4 * 151936 * 256 + 2 * es * 512 * 4096
     assert floor <= prep <= floor + 64 * 1024
     ws0 = xp.xp_workspace_bytes(w, 32, 0)
     ws1 = xp.xp_workspace_bytes(w, 32, 512)

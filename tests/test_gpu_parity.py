@@ -68,6 +68,30 @@ def test_hidden_cache(case):
     check_close(xh.cpu().numpy(), want, LAT_TOL[wl.dtype] / 4, "xh")
 
 
+def test_hidden_cache_fp32_grade(case):
+    # bf16 inputs, but every product of the hidden cache is carried in fp32: the folded
+    # projection keeps a hi + lo pair of bf16 planes, so a dropped lo plane (error near
+    # 2^-9 of |xh|) or a missing mean term fails this bound
+    wl, d, dev, p = case
+    xh = torch.empty(wl.N, wl.B, wl.r, dtype=torch.float32, device="cuda")
+    xp.xp_hidden_cache(dev.head.handle, dev.h, wl.N, xh, dev.ws)
+    check_close(xh.cpu().numpy(), _oracle_xh(d, wl, p), 2e-4 if wl.dtype == "bf16" else 1e-4,
+                "xh")
+
+
+def test_hidden_cache_unaligned_input(case):
+    # h_full one element past a 16-byte boundary cannot be tiled by TMA: the unfolded
+    # path runs and must agree to the same bound
+    wl, d, dev, p = case
+    buf = torch.empty(dev.h.numel() + 8, dtype=dev.h.dtype, device="cuda")
+    h1 = buf[1:1 + dev.h.numel()].view_as(dev.h)
+    h1.copy_(dev.h)
+    xh = torch.empty(wl.N, wl.B, wl.r, dtype=torch.float32, device="cuda")
+    xp.xp_hidden_cache(dev.head.handle, h1, wl.N, xh, dev.ws)
+    check_close(xh.cpu().numpy(), _oracle_xh(d, wl, p), 2e-4 if wl.dtype == "bf16" else 1e-4,
+                "xh")
+
+
 def test_latent(case):
     wl, d, dev, p = case
     xh_np = I.random_xh(wl, seed=7)
