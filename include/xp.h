@@ -52,7 +52,9 @@ typedef enum {
   XP_ECUDA = 4,         /* a CUDA runtime call failed (launch, copy, attribute)        */
   XP_EBADTOKEN = 5,     /* device flag: a token id outside [0, V) was clamped          */
   XP_ETIMEOUT = 6,      /* device flag: a bounded wait inside a kernel gave up         */
-  XP_EUNSUPPORTED = 7   /* shape not supported by this build                           */
+  XP_EUNSUPPORTED = 7,  /* shape not supported by this build                           */
+  XP_ERANGE = 8         /* device flag: a latent-stage value left the fp16 range of the
+                           tensor-core latent's exchanges (saturated; results unreliable) */
 } xp_status;
 
 typedef enum { XP_BF16 = 0, XP_F32 = 1 } xp_dtype;
@@ -124,6 +126,11 @@ xp_status xp_hidden_cache(const xp_head* head, const void* h_full, int N, float*
 /* Latent stage of one pass (all slots), written for slots 1..B-1:
  * blk: device [N, B] int64; am1: device [N] int64; xh: device [N, B, r] fp32;
  * lat: device [N, B-1, r] head dtype (written).
+ * Precision of the bf16 tensor-core path (r = 256, H = 512): the mixed latent u
+ * and the down projection's partial sums cross between CTAs as fp16 (relative
+ * error 2^-11, about a quarter of the bf16 output rounding); the SwiGLU
+ * activations are carried as bf16 hi + lo pairs; everything else is fp32.  A value
+ * outside the fp16 range saturates and raises XP_ERANGE.
  * xpress kernels page, _xpress_latent_kernel; qwen3_xpress page, _refine_latent. */
 xp_status xp_latent_pass(const xp_head* head, const int64_t* blk, const int64_t* am1,
                          const float* xh, int N, void* lat, cudaStream_t stream);
@@ -194,7 +201,7 @@ xp_status xp_jacobi_refine(const xp_head* head, const void* base, int64_t stride
                            void* ws, cudaStream_t stream);
 
 /* Synchronise `stream`, read and clear the head's device error word:
- * XP_OK, XP_EBADTOKEN or XP_ETIMEOUT (timeout wins when both are set). */
+ * XP_OK, XP_EBADTOKEN, XP_ERANGE or XP_ETIMEOUT (precedence in reverse order). */
 xp_status xp_get_error(const xp_head* head, cudaStream_t stream);
 
 /* Name of the readout kernel the head uses for its shape (for profiling). */

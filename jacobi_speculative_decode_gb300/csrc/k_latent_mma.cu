@@ -11,27 +11,37 @@
 // The cluster splits the work so each CTA holds only 1/8 of the weights: CTA q
 // owns channels [q*CS, (q+1)*CS), CS = r/8 (mixer, residual, output) and hidden
 // units [q*64, (q+1)*64) (SwiGLU).  Per group of MT rows (whole blocks):
-//   1. gather E rows and xh for the own channels (cp.async), x = xh + E[prev]
-//   2. u = per-channel causal mix of x (fp32), split into bf16 hi + lo
-//      (u = hi + lo to ~2^-17) and sent to every CTA of the cluster (itself
-//      included) with one bulk shared-to-shared copy per half and CTA; in the
-//      receivers the slice of CTA p is K-chunk p of a 64B-swizzled operand
-//   3. [gate | up] = u [w_gate ; w_up][own units]^T from hi and lo: tcgen05.mma
-//      (M = 128 rows, of which the group's MT are real, N = 128) into TMEM;
-//      a = silu(gate) * up, kept as bf16 hi + lo
-//   4. partial = a w_down[:, own units]^T for ALL r channels, tcgen05.mma again
-//      (w_down's column slice arrives by TMA into the u buffer, dead by then);
-//      each CS-channel piece goes to the CTA owning it by bulk copy
-//   5. lat = u + the 8 partials of the own channels, added in a fixed order
+//   1. x = xh + E[prev] for the own channels (every thread loads the token it needs)
+//   2. u = per-channel causal mix of x (fp32; item = slot b x channel pair), kept in
+//      fp32 for the residual and sent to the 7 peers as fp16 with one bulk copy each;
+//      the own slice stays in a buffer of its own, which nothing overwrites before
+//      the copies out of it are known to have landed
+//   3. [gate ; up] = [w_gate ; w_up][own units] u^T, tcgen05.mma kind::f16 on fp16
+//      operands (the head keeps fp16 copies of w_gate and w_up), the weights as the
+//      M = 128 side and the group's rows as N = MT; the weight rows are interleaved
+//      so that one TMEM lane quadrant holds gate and up of the same 16 units; as soon
+//      as the MMAs retire, w_down's column slice for the own units streams by TMA
+//      into the u buffer; a = silu(gate) * up as bf16 hi + lo
+//   4. partial = w_down[:, own units] a^T for ALL r channels (two M = 128 tiles, the
+//      activations' hi rows and lo rows side by side as N = 2*MT, summed when read
+//      back), staged by the warp whose lanes hold owner p's channels as
+//      [channel][row pair] fp16 and sent to owner p with one bulk copy
+//   5. lat = u + the 8 partials of the own channels, added in a fixed order (fp32)
+// The fp16 exchanges halve the bytes that cross the cluster network, whose
+// bandwidth per SM sets their latency; fp16's 2^-11 relative error is a quarter of
+// the bf16 rounding of the stored latent.  Values beyond the fp16 range saturate
+// and raise XP_ERR_RANGE.
 // The only cluster-wide barrier per group is a split arrive/wait that keeps a
-// CTA from sending into buffers a peer is still reading.
+// CTA from sending into buffers a peer is still reading; after its last group a
+// CTA arrives as soon as everything addressed to it has landed.
 //
 // Shared-memory operand layouts (what the TMA writes and tcgen05 reads):
 //   128B swizzle: element (row, k) of an R-row matrix, 64-column chunks, at
 //     (k/64)*R*128 + row*128 + ((((k%64)/8) ^ (row%8))*16) + (k%8)*2
-//   64B swizzle (the exchanged u): chunk p holds columns [32p, 32p+32) of MT rows,
-//     (row, c) at p*MT*64 + row*64 + (((c/8) ^ ((row/2)%4))*16) + (c%8)*2
+//   64B swizzle (the exchanged u, fp16): sender p's slice holds columns [32p, 32p+32)
+//     of MT rows: (row, c) at row*64 + (((c/8) ^ ((row/2)%4))*16) + (c%8)*2
 #include <cooperative_groups.h>
+#include <cuda_fp16.h>
 
 #include <algorithm>
 
@@ -47,12 +57,15 @@ namespace {
 constexpr int CL = 8;          // CTAs per cluster
 constexpr int THREADS = 256;   // 8 warps
 constexpr int HS = 64;         // own hidden units (H = 512)
-constexpr int CS = 32;         // own channels (r = 256)
+constexpr int CS = 32;         // own channels (r = 256) == warp size
 constexpr int R = CL * CS;     // latent rank handled by this kernel
+
+// bytes of one staged partial block: [CS channels][MT/2 + 1 row pairs] of fp16x2 (odd pitch)
+__host__ __device__ constexpr int blk_bytes(int MT) { return ((CS * (MT / 2 + 1) * 4 + 15) / 16) * 16; }
 
 struct Plan {                  // byte offsets into dynamic shared memory
   int MT;
-  int wgu, mix, ubuf, uout, ahi, alo, rcv, ex, xh, us, prev, bars;
+  int wgu, mix, ubuf, uout, act, rcv, sx, us, rowi, bars;
   int mix_rows;
   int total;
 };
@@ -70,19 +83,17 @@ __host__ __device__ inline Plan make_plan(int MT, int B) {
     o += bytes;
     return at;
   };
-  p.wgu = take((R / 64) * 128 * 128, 1024);     // [w_gate; w_up] own rows, 128B swizzle
+  p.wgu = take((R / 64) * 128 * 128, 1024);     // own w_gate / w_up rows (interleaved), 128B swizzle
   p.mix = take(mparts * mbox * CS * 2, 1024);
-  // u hi + lo (64B swizzle, 8 chunks each), later w_down[:, own] (R rows x 64, 128B
-  // swizzle), later the outgoing partial sums ([owner][MT][CS] fp32)
-  p.ubuf = take(std::max(std::max(2 * MT * R * 2, R * HS * 2), CL * MT * CS * 4), 1024);
-  p.uout = take(2 * MT * 64, 1024);             // own u slice, hi then lo
-  p.ahi = take(MT * 128, 1024);
-  p.alo = take(MT * 128, 1024);
-  p.rcv = take(CL * MT * CS * 4, 16);           // partial sums received, one slot per CTA
-  p.ex = take(MT * CS * 4, 16);                 // E[prev] rows, own channels
-  p.xh = take(MT * CS * 4, 16);
-  p.us = take(MT * (CS + 1) * 4, 16);
-  p.prev = take(MT * 8, 16);
+  // u (fp16) of the 8 senders (64B swizzle), later w_down[:, own] (R rows x 64, 128B
+  // swizzle), later the 7 outgoing partial blocks
+  p.ubuf = take(std::max(std::max(CL * MT * 64, R * HS * 2), (CL - 1) * blk_bytes(MT)), 1024);
+  p.uout = take(MT * 64, 1024);                 // own u: the MMA's and the peers' copy
+  p.act = take(2 * MT * 128, 1024);             // activations hi rows then lo rows, 64 units, 128B swizzle
+  p.rcv = take(CL * blk_bytes(MT), 16);         // partial blocks by sender (own one at slot q)
+  p.sx = take(MT * CS * 4, 16);                 // x = xh + E[prev], own channels
+  p.us = take(MT * CS * 4, 16);                 // u fp32, own channels (the residual)
+  p.rowi = take(MT * 4, 16);                    // lat row of each group row, -1 = not stored
   p.bars = take(64, 16);
   p.total = o;
   return p;
@@ -94,14 +105,7 @@ __device__ __forceinline__ int swz128(int row, int k, int Rr) {
 __device__ __forceinline__ int swz64(int row, int c) {      // within one 32-column chunk
   return row * 64 + ((((c >> 3) ^ ((row >> 1) & 3))) << 4) + ((c & 7) << 1);
 }
-// 16-byte chunk k of row m of a [rows][32] fp32 tile, rotated so that eight
-// consecutive rows writing the same logical chunk hit eight different banks
-__device__ __forceinline__ int rot32(int m, int k) { return m * 128 + (((k + m) & 7) << 4); }
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 __device__ __forceinline__ void fence_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -140,16 +144,105 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
 __device__ __forceinline__ void cluster_arrive() {
   asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 }
+// arrive without ordering this thread's earlier memory operations (exit protocol only:
+// every byte addressed to this CTA was already observed through its mbarriers)
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
 __device__ __forceinline__ void cluster_wait() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 __device__ __forceinline__ float silu_fast(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
+// fp16 pair with saturation at the largest finite value; flags a clipped input
+__device__ __forceinline__ __half2 to_half2_sat(float2 v, bool& clipped) {
+  constexpr float kMax = 65504.0f;
+  clipped |= fabsf(v.x) > kMax || fabsf(v.y) > kMax;
+  return __floats2half2_rn(fminf(fmaxf(v.x, -kMax), kMax), fminf(fmaxf(v.y, -kMax), kMax));
+}
+
+__device__ __forceinline__ void split_bf16(float v, bf16& hi, bf16& lo) {
+  hi = __float2bfloat16_rn(v);
+  lo = __float2bfloat16_rn(v - __bfloat162float(hi));
+}
+
+// n consecutive TMEM columns (n = 16, 24, 32 or 48) of this warp's 32 lanes
+template <int NC>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t ta, float (&out)[NC]) {
+  static_assert(NC == 16 || NC == 24 || NC == 32 || NC == 48, "column count");
+  if constexpr (NC >= 32) {
+    uint32_t a[32];
+    ptx::tmem_ld32(ta, a);
+    if constexpr (NC == 48) {
+      uint32_t b[16];
+      ptx::tmem_ld16(ta + 32, b);
+      ptx::tmem_wait_ld();
+#pragma unroll
+      for (int i = 0; i < 16; ++i) out[32 + i] = __uint_as_float(b[i]);
+    } else {
+      ptx::tmem_wait_ld();
+    }
+#pragma unroll
+    for (int i = 0; i < 32; ++i) out[i] = __uint_as_float(a[i]);
+  } else {
+    uint32_t a[16];
+    ptx::tmem_ld16(ta, a);
+    if constexpr (NC == 24) {
+      uint32_t b[8];
+      ptx::tmem_ld8(ta + 16, b);
+      ptx::tmem_wait_ld();
+#pragma unroll
+      for (int i = 0; i < 8; ++i) out[16 + i] = __uint_as_float(b[i]);
+    } else {
+      ptx::tmem_wait_ld();
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) out[i] = __uint_as_float(a[i]);
+  }
+}
+
 struct Maps {
-  CUtensorMap wg, wu, wdk, mix;
+  CUtensorMap wgu, wdk, mix;
 };
 
-constexpr uint32_t TMEM_COLS = 512;    // [gate | up] 128 | partial sums 256
+// u[bl*B + b][c] = sum_{j <= b} mix[b][j][c] x[bl*B + j][c] for blocks bl0 .. bl0+nbv-1
+// (nbv <= NB), one item = (slot b, channel pair); the mixer value is loaded once and
+// used for every block.  Writes u (fp32) and its fp16 copy for the exchange.  With
+// PARTIAL, blocks k >= nbv are neither read nor written (nbv < NB); without it nbv == NB.
+template <int NB, bool PARTIAL = false>
+__device__ __forceinline__ void mix_slots(const bf16* __restrict__ sMix, const float* sX, float* sUs,
+                                          uint8_t* uh, int B, int nbv, int tid, bool& out_of_range,
+                                          int bl0 = 0) {
+  for (int it = tid; it < B * (CS / 2); it += THREADS) {
+    const int b = it / (CS / 2), c = (it % (CS / 2)) * 2;
+    const bf16* mrow = sMix + (b * B) * CS + c;
+    const float* xr = sX + (bl0 * B) * CS + c;
+    float2 acc[NB];
+#pragma unroll
+    for (int k = 0; k < NB; ++k) acc[k] = make_float2(0.f, 0.f);
+#pragma unroll 4
+    for (int j = 0; j <= b; ++j) {
+      const float2 mv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(mrow + j * CS));
+#pragma unroll
+      for (int k = 0; k < NB; ++k) {
+        if (PARTIAL && k >= nbv) break;
+        const float2 xv = *reinterpret_cast<const float2*>(xr + (k * B + j) * CS);
+        acc[k].x = fmaf(mv.x, xv.x, acc[k].x);
+        acc[k].y = fmaf(mv.y, xv.y, acc[k].y);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < NB; ++k)
+      if (k < nbv) {
+        const int m = (bl0 + k) * B + b;
+        *reinterpret_cast<float2*>(sUs + m * CS + c) = acc[k];
+        *reinterpret_cast<__half2*>(uh + swz64(m, c)) = to_half2_sat(acc[k], out_of_range);
+      }
+  }
+}
+
+// [gate ; up] (hi columns then lo columns) at 0, the two partial tiles at 128 and 256
+constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t COL_GU = 0, COL_P = 128;
 
 template <int MTILES>
@@ -158,55 +251,58 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1) latent_
     const int64_t* __restrict__ am1, const float* __restrict__ xh, const float* __restrict__ E,
     bf16* __restrict__ lat, int N, int B, int V, uint32_t* err) {
   constexpr int MT = MTILES * 16;
+  constexpr int HALF = MT / 2;             // TMEM columns per reader warp in the SwiGLU step
+  constexpr int LDH = MT / 2 + 1;          // row pitch of a staged partial block (fp16x2 words)
+  constexpr int BLK = blk_bytes(MT);
+  constexpr uint32_t SLICE = MT * 64;      // bytes of one sender's u
   extern __shared__ uint8_t sm_raw[];
   uint8_t* sm = sm_raw + ((1024u - (ptx::smem_u32(sm_raw) & 1023u)) & 1023u);
   const int q = (int)cg::this_cluster().block_rank();
   const int cid = blockIdx.x / CL, nclusters = gridDim.x / CL;
   const Plan P = make_plan(MT, B);
   const uint32_t s0 = ptx::smem_u32(sm);
-  const uint32_t aW = s0 + P.wgu, aU = s0 + P.ubuf, aUo = s0 + P.uout;
-  const uint32_t aUhi = aU, aUlo = aU + MT * R * 2;
-  const uint32_t aAhi = s0 + P.ahi, aAlo = s0 + P.alo;
+  const uint32_t aW = s0 + P.wgu, aU = s0 + P.ubuf;
+  const uint32_t aAct = s0 + P.act;
   const bf16* sMix = (const bf16*)(sm + P.mix);
-  const float* sEx = (const float*)(sm + P.ex);
-  const float* sXh = (const float*)(sm + P.xh);
-  const uint8_t* sRcv = sm + P.rcv;
-  const uint8_t* sStage = sm + P.ubuf;     // outgoing partial sums, [owner][MT rows][CS]
+  float* sX = (float*)(sm + P.sx);
   float* sUs = (float*)(sm + P.us);
-  int64_t* sPrev = (int64_t*)(sm + P.prev);
+  int* sRow = (int*)(sm + P.rowi);
+  const uint32_t* sRcv = (const uint32_t*)(sm + P.rcv);
   const uint32_t bar_w = s0 + P.bars, bar_wd = bar_w + 8, bar_u = bar_w + 16, bar_p = bar_w + 24;
   const uint32_t bar_mma = bar_w + 32;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + P.bars + 40);
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   const int nb = MT / B;                   // blocks per group
   const int groups = (N + nb - 1) / nb;
-  const int ldp = CS + 1;
-  const uint32_t slice = MT * 64;          // bytes of one u half of one CTA
-  const uint32_t u_bytes_in = (uint32_t)(CL * 2 * slice);
-  const uint32_t p_bytes_in = (uint32_t)((CL - 1) * MT * CS * 4);
+  const uint32_t u_bytes_in = (uint32_t)((CL - 1) * SLICE);
+  const uint32_t p_bytes_in = (uint32_t)((CL - 1) * BLK);
   const uint64_t pol = ptx::policy_evict_last();
 
-  // ---- set-up: barriers, TMEM, then the resident weight and mixer slices by TMA ----
-  if (tid == 0) {
-    ptx::mbar_init(bar_w, 1);
-    ptx::mbar_init(bar_wd, 1);
-    ptx::mbar_init(bar_u, 1);
-    ptx::mbar_init(bar_p, 1);
-    ptx::mbar_init(bar_mma, 1);
-    ptx::fence_barrier_init();
-    const int mparts = (P.mix_rows + 255) / 256, mbox = std::min(P.mix_rows, 256);
-    ptx::mbar_arrive_expect_tx(bar_w, 2 * HS * R * 2 + mparts * mbox * CS * 2);
-    for (int kc = 0; kc < R / 64; ++kc) {
-      ptx::tma_load_2d(aW + kc * 16384, &maps.wg, bar_w, kc * 64, q * HS, pol);
-      ptx::tma_load_2d(aW + kc * 16384 + 8192, &maps.wu, bar_w, kc * 64, q * HS, pol);
-    }
-    for (int pt = 0; pt < mparts; ++pt)
-      ptx::tma_load_2d(s0 + P.mix + pt * mbox * CS * 2, &maps.mix, bar_w, q * CS, pt * mbox, pol);
-    // the first group's incoming u halves and partial sums
-    ptx::mbar_arrive_expect_tx(bar_u, u_bytes_in);
-    ptx::mbar_arrive_expect_tx(bar_p, p_bytes_in);
-  }
+  // ---- set-up: barriers, the resident weight and mixer slices by TMA (one box per
+  // lane of warp 0), TMEM (warp 1) ----
   if (warp == 0) {
+    if (lane == 0) {
+      ptx::mbar_init(bar_w, 1);
+      ptx::mbar_init(bar_wd, 1);
+      ptx::mbar_init(bar_u, 1);
+      ptx::mbar_init(bar_p, 1);
+      ptx::mbar_init(bar_mma, 1);
+      ptx::fence_barrier_init();
+      const int mparts = (P.mix_rows + 255) / 256, mbox = std::min(P.mix_rows, 256);
+      ptx::mbar_arrive_expect_tx(bar_w, 2 * HS * R * 2 + mparts * mbox * CS * 2);
+      for (int pt = 0; pt < mparts; ++pt)
+        ptx::tma_load_2d(s0 + P.mix + pt * mbox * CS * 2, &maps.mix, bar_w, q * CS, pt * mbox,
+                         pol);
+      // the first group's incoming u and partial blocks
+      ptx::mbar_arrive_expect_tx(bar_u, u_bytes_in);
+      ptx::mbar_arrive_expect_tx(bar_p, p_bytes_in);
+    }
+    __syncwarp();
+    // the head keeps [w_gate ; w_up] in this CTA's row order (see xp_launch_gu_to_f16):
+    // one 128-row box per 64-wide k chunk
+    if (lane < R / 64)
+      ptx::tma_load_2d(aW + lane * 16384, &maps.wgu, bar_w, lane * 64, q * 128, pol);
+  } else if (warp == 1) {
     ptx::tmem_alloc(ptx::smem_u32(s_tmem), TMEM_COLS);
     ptx::tmem_relinquish();
   }
@@ -223,240 +319,235 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1) latent_
     ptx::mbar_wait(bar_w, 0, &no_abort, err);
   }
   uint32_t mma_phase = 0;
-  // TMEM readers: warps whose lane quadrant holds real rows (MT <= 64), two column halves
-  const bool reader = (warp & 3) * 32 < MT;
   const int quad = warp & 3, half = warp >> 2;
-  const int trow = quad * 32 + lane;        // this thread's row when it is a reader
 
   int it = 0;
   for (int grp = cid; grp < groups; grp += nclusters, ++it) {
     const uint32_t ph = it & 1;
+    const bool last = grp + nclusters >= groups;
     const int n0 = grp * nb;
     const int rows = std::min(nb, N - n0) * B;   // valid rows of this group
 
-    // ---- 1. token ids, then E[prev] and xh for the own channels ----
-    for (int m = tid; m < MT; m += THREADS) {
-      int64_t t = 0;
-      if (m < rows) {
-        const int n = n0 + m / B, b = m % B;
-        t = checked_token(b == 0 ? am1[n] : blk[(int64_t)n * B + b - 1], V, err);
+    // ---- 1. x = xh + E[prev] for the own channels: row m, 4 channels per item ----
+    for (int m = tid; m < MT; m += THREADS)
+      sRow[m] = (m < rows && m % B != 0) ? (n0 + m / B) * (B - 1) + m % B - 1 : -1;
+    for (int i0 = tid; i0 < MT * (CS / 4); i0 += 2 * THREADS) {
+      float4 e[2], xv[2];
+      int mm[2];
+      int64_t tok[2];
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {       // token ids and xh first, both in flight together
+        const int i = i0 + k * THREADS;
+        const int m = i / (CS / 4), c4 = (i % (CS / 4)) * 4;
+        mm[k] = i < MT * (CS / 4) ? m : -1;
+        e[k] = xv[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        tok[k] = 0;
+        if (mm[k] >= 0 && m < rows) {
+          const int n = n0 + m / B, b = m % B;
+          tok[k] = b == 0 ? am1[n] : blk[(int64_t)n * B + b - 1];
+          xv[k] = __ldg(reinterpret_cast<const float4*>(xh + (int64_t)(n0 * B + m) * R + q * CS + c4));
+        }
       }
-      sPrev[m] = t;
-    }
-    __syncthreads();
-    for (int i = tid; i < MT * 2 * (CS / 4); i += THREADS) {
-      const int m = i / (2 * (CS / 4)), c = i % (2 * (CS / 4));
-      const int cc = c % (CS / 4);
-      const bool is_e = c < CS / 4;
-      const uint32_t dst = s0 + (is_e ? P.ex : P.xh) + (m * CS + cc * 4) * 4;
-      if (m < rows) {
-        const float* src = is_e ? E + sPrev[m] * R + q * CS + cc * 4
-                                : xh + ((int64_t)(n0 * B + m)) * R + q * CS + cc * 4;
-        cp_async16(dst, src);
-      } else {
-        *reinterpret_cast<uint4*>(sm + (dst - s0)) = make_uint4(0, 0, 0, 0);
-      }
-    }
-    cp_async_wait_all();
-    __syncthreads();
-
-    // ---- 2. x = xh + E[prev]; u = per-channel causal mix (fp32); send u hi/lo ----
-    for (int i = tid; i < MT * CS; i += THREADS) {
-      const int m = i / CS, c = i % CS;
-      sUs[m * ldp + c] = sXh[m * CS + c] + sEx[m * CS + c];
+#pragma unroll
+      for (int k = 0; k < 2; ++k)
+        if (mm[k] >= 0 && mm[k] < rows) {
+          const int c4 = ((i0 + k * THREADS) % (CS / 4)) * 4;
+          const int64_t t = checked_token(tok[k], V, err);
+          e[k] = __ldg(reinterpret_cast<const float4*>(E + t * R + q * CS + c4));
+        }
+#pragma unroll
+      for (int k = 0; k < 2; ++k)
+        if (mm[k] >= 0) {
+          const int i = i0 + k * THREADS;
+          *reinterpret_cast<float4*>(sX + mm[k] * CS + (i % (CS / 4)) * 4) =
+              make_float4(e[k].x + xv[k].x, e[k].y + xv[k].y, e[k].z + xv[k].z, e[k].w + xv[k].w);
+        }
     }
     __syncthreads();
     // the previous group's peers are done reading this CTA's buffers, and it theirs
     if (it > 0) cluster_wait();
-    float uown[8];
-    const int wm = tid / (CS / 8), wc0 = (tid % (CS / 8)) * 8;   // one 8-channel run each
-    const bool mixer = tid < MT * CS / 8;
-    if (mixer) {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) uown[e] = 0.f;
-      if (wm < rows) {
-        const int bl = wm / B, b = wm % B;
-#pragma unroll 4
-        for (int j = 0; j < B; ++j) {
-          const uint4 mv = *reinterpret_cast<const uint4*>(sMix + (b * B + j) * CS + wc0);
-          const bf16* mj = reinterpret_cast<const bf16*>(&mv);
-          const float* xj = sUs + (bl * B + j) * ldp + wc0;
-#pragma unroll
-          for (int e = 0; e < 8; ++e) uown[e] = fmaf(__bfloat162float(mj[e]), xj[e], uown[e]);
-        }
-      }
-      uint32_t hi[4], lo[4];
-#pragma unroll
-      for (int e = 0; e < 8; e += 2) {
-        const __nv_bfloat162 h2 = __floats2bfloat162_rn(uown[e], uown[e + 1]);
-        const float2 hf = __bfloat1622float2(h2);
-        const __nv_bfloat162 l2 = __floats2bfloat162_rn(uown[e] - hf.x, uown[e + 1] - hf.y);
-        hi[e / 2] = *reinterpret_cast<const uint32_t*>(&h2);
-        lo[e / 2] = *reinterpret_cast<const uint32_t*>(&l2);
-      }
-      const int off = swz64(wm, wc0);
-      *reinterpret_cast<uint4*>(sm + P.uout + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-      *reinterpret_cast<uint4*>(sm + P.uout + slice + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-    }
-    fence_async_smem();                    // the bulk copies read u_out
-    __syncthreads();                       // every x read before u (fp32) replaces it
-    if (tid == 0) {
-      for (int dp = 0; dp < CL; ++dp) {
-        const int p = (q + dp) % CL;       // itself first
-        const uint32_t rb = mapa(bar_u, p);
-        ptx::bulk_copy_to_peer(mapa(aUhi + q * slice, p), aUo, slice, rb);
-        ptx::bulk_copy_to_peer(mapa(aUlo + q * slice, p), aUo + slice, slice, rb);
-      }
-    }
-    if (mixer) {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) sUs[wm * ldp + wc0 + e] = uown[e];
-    }
-    mbar_wait_cluster(bar_u, ph, err);
 
-    // ---- 3. [gate | up] from u = hi + lo (tcgen05, fp32 in TMEM); a = silu(g) * up ----
-    if (tid == 0) {
-      ptx::tc_fence_after();
-      constexpr uint32_t ID = ptx::idesc_bf16_f32(128, 128);
-      for (int s = 0; s < R / 16; ++s) {
-        const uint64_t bw = ptx::sw128_desc(aW + (s / 4) * 16384 + (s % 4) * 32);
-        const uint32_t ao = (s / 2) * slice + (s % 2) * 32;
-        ptx::mma_bf16(tmem + COL_GU, ptx::sw64_desc(aUhi + ao), bw, ID, s != 0);
-        ptx::mma_bf16(tmem + COL_GU, ptx::sw64_desc(aUlo + ao), bw, ID, 1);
-      }
-      ptx::mma_commit(bar_mma);
-    }
+    // ---- 2. u = per-channel causal mix (fp32): item = (slot b, channel pair) ----
     {
-      volatile int no_abort = 0;
-      ptx::mbar_wait(bar_mma, mma_phase, &no_abort, err);
-      mma_phase ^= 1;
-    }
-    ptx::tc_fence_after();
-    if (reader) {
-      // each reader thread: its row, 32 of the 64 own hidden units (gate and up)
-      uint32_t g[32], v[32];
-      const uint32_t ta = tmem + ((uint32_t)(quad * 32) << 16) + COL_GU + half * 32;
-      ptx::tmem_ld32(ta, g);
-      ptx::tmem_ld32(ta + HS, v);
-      ptx::tmem_wait_ld();
-      if (trow < MT) {
-#pragma unroll
-        for (int c8 = 0; c8 < 4; ++c8) {
-          uint32_t hw[4], lw[4];
-#pragma unroll
-          for (int e = 0; e < 8; e += 2) {
-            const int k = c8 * 8 + e;
-            const float a0 = silu_fast(__uint_as_float(g[k])) * __uint_as_float(v[k]);
-            const float a1 = silu_fast(__uint_as_float(g[k + 1])) * __uint_as_float(v[k + 1]);
-            const __nv_bfloat162 h2 = __floats2bfloat162_rn(a0, a1);
-            const float2 hf = __bfloat1622float2(h2);
-            const __nv_bfloat162 l2 = __floats2bfloat162_rn(a0 - hf.x, a1 - hf.y);
-            hw[e / 2] = *reinterpret_cast<const uint32_t*>(&h2);
-            lw[e / 2] = *reinterpret_cast<const uint32_t*>(&l2);
-          }
-          const int off = swz128(trow, half * 32 + c8 * 8, MT);
-          *reinterpret_cast<uint4*>(sm + P.ahi + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-          *reinterpret_cast<uint4*>(sm + P.alo + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-        }
+      uint8_t* uh = sm + P.uout;                     // own u (fp16)
+      bool out_of_range = false;
+      switch (nb) {
+        case 1: mix_slots<1>(sMix, sX, sUs, uh, B, 1, tid, out_of_range); break;
+        case 2: mix_slots<2>(sMix, sX, sUs, uh, B, 2, tid, out_of_range); break;
+        case 3: mix_slots<3>(sMix, sX, sUs, uh, B, 3, tid, out_of_range); break;
+        case 4: mix_slots<4>(sMix, sX, sUs, uh, B, 4, tid, out_of_range); break;
+        case 6: mix_slots<6>(sMix, sX, sUs, uh, B, 6, tid, out_of_range); break;
+        default:
+          for (int bl0 = 0; bl0 < nb; bl0 += 4)
+            mix_slots<4, true>(sMix, sX, sUs, uh, B, std::min(4, nb - bl0), tid, out_of_range,
+                               bl0);
+      }
+      if (out_of_range) atomicOr(err, XP_ERR_RANGE);
+      // rows past the last whole block of the group read as zero
+      for (int m = nb * B + warp; m < MT; m += THREADS / 32) {
+        sUs[m * CS + lane] = 0.f;
+        *reinterpret_cast<__half*>(uh + swz64(m, lane)) = __float2half_rn(0.f);
       }
     }
-    ptx::tc_fence_before();
-    fence_async_smem();                    // activations seen by the next MMA
-    __syncthreads();                       // u is dead: w_down's slice may overwrite it
-    if (tid == 0) {
-      ptx::mbar_arrive_expect_tx(bar_wd, R * HS * 2);
-      ptx::tma_load_2d(aU, &maps.wdk, bar_wd, q * HS, 0, pol);
-    }
-    {
-      volatile int no_abort = 0;
-      ptx::mbar_wait(bar_wd, ph, &no_abort, err);
-    }
-
-    // ---- 4. partial down projection over own units (tcgen05), sent to each owner ----
-    if (tid == 0) {
-      ptx::tc_fence_after();
-      constexpr uint32_t ID = ptx::idesc_bf16_f32(128, R);
-      for (int kk = 0; kk < 4; ++kk) {
-        const uint64_t bw = ptx::sw128_desc(aU + kk * 32);
-        ptx::mma_bf16(tmem + COL_P, ptx::sw128_desc(aAhi + kk * 32), bw, ID, kk != 0);
-        ptx::mma_bf16(tmem + COL_P, ptx::sw128_desc(aAlo + kk * 32), bw, ID, 1);
-      }
-      ptx::mma_commit(bar_mma);
-    }
-    {
-      volatile int no_abort = 0;
-      ptx::mbar_wait(bar_mma, mma_phase, &no_abort, err);
-      mma_phase ^= 1;
-    }
-    ptx::tc_fence_after();
-    if (reader) {
-      // each reader thread: its row, owners [4*half, 4*half+4) (CS = 32 channels each)
-      const uint32_t ta = tmem + ((uint32_t)(quad * 32) << 16) + COL_P;
-#pragma unroll 1
-      for (int p = half * 4; p < half * 4 + 4; ++p) {
-        uint32_t pv[32];
-        ptx::tmem_ld32(ta + p * CS, pv);
-        ptx::tmem_wait_ld();
-        if (trow < MT) {
-          uint8_t* dst = sm + P.ubuf + p * MT * CS * 4;
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            *reinterpret_cast<uint4*>(dst + rot32(trow, k)) =
-                make_uint4(pv[4 * k], pv[4 * k + 1], pv[4 * k + 2], pv[4 * k + 3]);
-        }
-      }
-    }
-    ptx::tc_fence_before();
-    fence_async_smem();                    // the bulk copies read the staged partial sums
+    fence_async_smem();                    // the bulk copies and the MMA read u
     __syncthreads();
     if (tid == 0) {
       for (int dp = 1; dp < CL; ++dp) {
         const int p = (q + dp) % CL;
-        ptx::bulk_copy_to_peer(mapa(s0 + P.rcv + q * MT * CS * 4, p), aU + p * MT * CS * 4,
-                               MT * CS * 4, mapa(bar_p, p));
+        ptx::bulk_copy_to_peer(mapa(aU + q * SLICE, p), s0 + P.uout, SLICE, mapa(bar_u, p));
+      }
+    }
+    mbar_wait_cluster(bar_u, ph, err);
+
+    // ---- 3. [gate ; up] (units x rows) from u = hi + lo; w_down streams in behind ----
+    if (tid == 0) {
+      ptx::tc_fence_after();
+      constexpr uint32_t ID = ptx::idesc_f16_f32(128, MT);
+      const uint64_t dw = ptx::sw128_desc(aW), du = ptx::sw64_desc(aU);
+      const uint64_t dq = ptx::sw64_desc(s0 + P.uout);
+#pragma unroll
+      for (int s = 0; s < R / 16; ++s) {
+        const int p = s / 2;               // sender of channels [32p, 32p + 32)
+        const uint64_t bd = (p == q ? dq : du + ((p * SLICE) >> 4)) + (s % 2) * 2;
+        ptx::mma_bf16(tmem + COL_GU, dw + (((s / 4) * 16384 + (s % 4) * 32) >> 4), bd, ID, s != 0);
+      }
+      ptx::mma_commit(bar_mma);
+      volatile int no_abort = 0;
+      ptx::mbar_wait(bar_mma, mma_phase, &no_abort, err);
+      // u is dead: w_down's column slice for the own units goes into its buffer
+      ptx::mbar_arrive_expect_tx(bar_wd, R * HS * 2);
+      ptx::tma_load_2d(aU, &maps.wdk, bar_wd, q * HS, 0, pol);
+    } else {
+      volatile int no_abort = 0;
+      ptx::mbar_wait(bar_mma, mma_phase, &no_abort, err);
+    }
+    mma_phase ^= 1;
+    ptx::tc_fence_after();
+    {
+      // warp (quad g, half h): TMEM lanes 32g.. hold gate (lanes 0-15) and up (16-31) of
+      // units 16g..16g+15, for the rows (columns) [h*HALF, (h+1)*HALF); the two lane
+      // halves swap values so that each computes HALF/2 rows of all 16 units
+      float v[HALF];
+      tmem_ld_cols<HALF>(tmem + ((uint32_t)(quad * 32) << 16) + COL_GU + half * HALF, v);
+      const bool lo_lane = lane < 16;
+      const int unit = quad * 16 + (lane & 15);
+#pragma unroll
+      for (int i = 0; i < HALF / 2; ++i) {
+        const float other = __shfl_xor_sync(0xFFFFFFFFu, lo_lane ? v[i + HALF / 2] : v[i], 16);
+        const float gate = lo_lane ? v[i] : other;
+        const float up = lo_lane ? other : v[i + HALF / 2];
+        const int m = half * HALF + (lo_lane ? i : HALF / 2 + i);
+        const float a = silu_fast(gate) * up;
+        bf16 hi, lo;
+        split_bf16(a, hi, lo);
+        const int off = swz128(m, unit, MT);
+        *reinterpret_cast<bf16*>(sm + P.act + off) = hi;
+        *reinterpret_cast<bf16*>(sm + P.act + MT * 128 + off) = lo;
+      }
+    }
+    ptx::tc_fence_before();
+    fence_async_smem();                    // activations seen by the next MMA
+    __syncthreads();
+
+    // ---- 4. partial down projection over own units, channels x rows (two M tiles) ----
+    if (tid == 0) {
+      volatile int no_abort = 0;
+      ptx::mbar_wait(bar_wd, ph, &no_abort, err);
+      ptx::tc_fence_after();
+      constexpr uint32_t ID = ptx::idesc_bf16_f32(128, 2 * MT);
+      const uint64_t dw = ptx::sw128_desc(aU), da = ptx::sw128_desc(aAct);
+#pragma unroll
+      for (int t = 0; t < R / 128; ++t)
+#pragma unroll
+        for (int kk = 0; kk < HS / 16; ++kk)
+          ptx::mma_bf16(tmem + COL_P + t * 128, dw + ((t * 16384 + kk * 32) >> 4), da + kk * 2, ID,
+                        kk != 0);
+      ptx::mma_commit(bar_mma);
+    }
+    {
+      volatile int no_abort = 0;
+      ptx::mbar_wait(bar_mma, mma_phase, &no_abort, err);
+      mma_phase ^= 1;
+    }
+    ptx::tc_fence_after();
+    {
+      // warp p stages owner p's block: its lanes hold channels 32p.. of tile p / 4
+      const int p = warp;
+      const uint32_t ta = tmem + ((uint32_t)(quad * 32) << 16) + COL_P + (p >> 2) * 128;
+      uint32_t* dst = p == q ? (uint32_t*)(sm + P.rcv + q * BLK)
+                             : (uint32_t*)(sm + P.ubuf + ((p - q - 1 + CL) % CL) * BLK);
+      bool out_of_range = false;
+#pragma unroll
+      for (int c0 = 0; c0 < MT; c0 += 16) {
+        float vh[16], vl[16];
+        tmem_ld_cols<16>(ta + c0, vh);
+        tmem_ld_cols<16>(ta + MT + c0, vl);
+#pragma unroll
+        for (int i = 0; i < 16; i += 2) {
+          const __half2 h2 =
+              to_half2_sat(make_float2(vh[i] + vl[i], vh[i + 1] + vl[i + 1]), out_of_range);
+          dst[lane * LDH + (c0 + i) / 2] = *reinterpret_cast<const uint32_t*>(&h2);
+        }
+      }
+      if (out_of_range) atomicOr(err, XP_ERR_RANGE);
+    }
+    ptx::tc_fence_before();
+    fence_async_smem();                    // the bulk copies read the staged blocks
+    __syncthreads();
+    if (tid == 0) {
+      for (int dp = 1; dp < CL; ++dp) {
+        const int p = (q + dp) % CL;
+        ptx::bulk_copy_to_peer(mapa(s0 + P.rcv + q * BLK, p), aU + (dp - 1) * BLK, BLK,
+                               mapa(bar_p, p));
       }
     }
     mbar_wait_cluster(bar_p, ph, err);
+    // everything addressed to this CTA has landed: after its last group it can
+    // release the peers' exit barrier now
+    if (last) cluster_arrive_relaxed();
 
     // ---- 5. lat (own channels) = u + sum_p partial_p, p = 0..7 in order ----
-    for (int i = tid; i < MT * CS; i += THREADS) {
-      const int m = i / CS, c = i % CS;
-      if (m < rows && (m % B) != 0) {
-        float v = sUs[m * ldp + c];
-        const int o = rot32(m, c >> 2) + (c & 3) * 4;
+    for (int i = tid; i < (MT / 2) * CS; i += THREADS) {
+      const int mp = i / CS, c = i % CS, m0 = 2 * mp;
+      const int r0 = sRow[m0], r1 = sRow[m0 + 1];
+      float v0 = sUs[m0 * CS + c], v1 = sUs[(m0 + 1) * CS + c];
 #pragma unroll
-        for (int p = 0; p < CL; ++p) {
-          const uint8_t* src = (p == q) ? sStage + q * MT * CS * 4 : sRcv + p * MT * CS * 4;
-          v += *reinterpret_cast<const float*>(src + o);
-        }
-        const int n = n0 + m / B, b = m % B;
-        lat[((int64_t)n * (B - 1) + b - 1) * R + q * CS + c] = __float2bfloat16_rn(v);
+      for (int p = 0; p < CL; ++p) {
+        const uint32_t w = sRcv[p * (BLK / 4) + c * LDH + mp];
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w));
+        v0 += f.x;
+        v1 += f.y;
       }
+      if (r0 >= 0) lat[(int64_t)r0 * R + q * CS + c] = __float2bfloat16_rn(v0);
+      if (r1 >= 0) lat[(int64_t)r1 * R + q * CS + c] = __float2bfloat16_rn(v1);
     }
-    __syncthreads();
-    // arm the next group's receive barriers, then tell the peers this CTA's
-    // buffers (u, w_down slice, staged and received partial sums) are free again
-    if (tid == 0 && grp + nclusters < groups) {
-      ptx::mbar_arrive_expect_tx(bar_u, u_bytes_in);
-      ptx::mbar_arrive_expect_tx(bar_p, p_bytes_in);
+    if (!last) {
+      __syncthreads();
+      // arm the next group's receive barriers, then tell the peers this CTA's
+      // buffers (u, w_down slice, staged and received partials) are free again
+      if (tid == 0) {
+        ptx::mbar_arrive_expect_tx(bar_u, u_bytes_in);
+        ptx::mbar_arrive_expect_tx(bar_p, p_bytes_in);
+      }
+      cluster_arrive();
     }
-    cluster_arrive();
   }
   cluster_wait();   // no CTA leaves while a peer may still send into it
-  if (warp == 0) {
+  if (warp == 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, TMEM_COLS);
   }
 }
 
-int g_max_clusters[2] = {0, 0};   // co-resident clusters per variant (queried once)
+// co-resident clusters per variant, queried once per shared-memory size
+int g_max_clusters[2] = {0, 0}, g_max_clusters_smem[2] = {0, 0};
 
 size_t smem_bytes(int MT, int B) { return (size_t)make_plan(MT, B).total + 1024; }
 
 template <int MTILES>
 int max_clusters(int smem) {
   int& cached = g_max_clusters[MTILES - 2];
-  if (cached > 0) return cached;
+  if (cached > 0 && g_max_clusters_smem[MTILES - 2] == smem) return cached;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(CL);
   cfg.blockDim = dim3(THREADS);
@@ -467,6 +558,7 @@ int max_clusters(int smem) {
       cudaOccupancyMaxActiveClusters(&n, latent_mma_kernel<MTILES>, &cfg) != cudaSuccess || n <= 0)
     n = 1;
   cached = n;
+  g_max_clusters_smem[MTILES - 2] = smem;
   return n;
 }
 
@@ -481,7 +573,7 @@ cudaError_t launch(const xp_head* h, const int64_t* blk, const int64_t* am1, con
   const int nb = MT / h->B;
   const int groups = (N + nb - 1) / nb;
   const int clusters = std::min(groups, max_clusters<MTILES>(smem));
-  const Maps maps = {h->tm_wg, h->tm_wu, h->tm_wd, h->tm_mixT};
+  const Maps maps = {h->tm_wgu, h->tm_wd, h->tm_mixT};
   e = xp_launch_pdl(latent_mma_kernel<MTILES>, dim3(clusters * CL), dim3(THREADS), (size_t)smem,
                     s, maps, blk, am1, xh, (const float*)h->E, (bf16*)lat, N, h->B, h->V, h->err);
   return e != cudaSuccess ? e : cudaGetLastError();
@@ -492,7 +584,7 @@ cudaError_t launch(const xp_head* h, const int64_t* blk, const int64_t* am1, con
 bool xp_latent_mma_ok(int r, int H, int B, xp_dtype dt) {
   // the production shape of the head: r = 256 (32 channels per CTA), H = 512 (64 units)
   if (dt != XP_BF16 || B < 2 || B > 32 || r != R || H != CL * HS) return false;
-  return smem_bytes(48, B) <= 227 * 1024;
+  return smem_bytes(32, B) <= 227 * 1024;
 }
 
 // Tensor maps of the weight and mixer slices (2-D, bf16).
@@ -501,19 +593,18 @@ bool xp_latent_mma_maps(xp_head* h) {
   if (!fn) return false;
   const int B = h->B;
   auto enc = [&](CUtensorMap* m, const void* ptr, int rows, int cols, int box_c, int box_r,
-                 bool swz128) {
+                 bool swz128, CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
     const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
     const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
     const cuuint32_t box[2] = {(cuuint32_t)box_c, (cuuint32_t)box_r};
     const cuuint32_t es[2] = {1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
-              es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+    return fn(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE,
               swz128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
            CUDA_SUCCESS;
   };
-  return enc(&h->tm_wg, h->w_gate, CL * HS, R, 64, HS, true) &&
-         enc(&h->tm_wu, h->w_up, CL * HS, R, 64, HS, true) &&
+  return enc(&h->tm_wgu, h->wgu16, CL * 128, R, 64, 128, true, CU_TENSOR_MAP_DATA_TYPE_FLOAT16) &&
          enc(&h->tm_wd, h->w_down, R, CL * HS, 64, R, true) &&
          enc(&h->tm_mixT, h->mixT, B * B, R, CS, std::min(B * B, 256), false);
 }
@@ -522,7 +613,38 @@ cudaError_t xp_launch_latent_mma(const xp_head* h, const int64_t* blk, const int
                                  const float* xh, int N, void* lat, cudaStream_t s) {
   // 32-row groups while they fit in one wave of co-resident clusters, else 48-row groups
   const int groups32 = (N + 32 / h->B - 1) / (32 / h->B);
-  if (groups32 <= max_clusters<2>((int)smem_bytes(32, h->B)))
+  if (groups32 <= max_clusters<2>((int)smem_bytes(32, h->B)) ||
+      smem_bytes(48, h->B) > 227 * 1024)
     return launch<2>(h, blk, am1, xh, N, lat, s);
   return launch<3>(h, blk, am1, xh, N, lat, s);
+}
+
+namespace {
+// [w_gate ; w_up] (bf16) -> fp16 with saturation (exact for magnitudes in fp16's normal
+// range), rows reordered for the cluster latent: CTA q's 128 rows are, for g = 0..3,
+// gate units q*64 + 16g .. +15 then up units q*64 + 16g .. +15, so that TMEM lane
+// quadrant g of its [gate ; up] accumulator holds both halves of 16 units.
+__global__ void gu_to_f16_kernel(const bf16* __restrict__ wg, const bf16* __restrict__ wu,
+                                 __half* __restrict__ out, int rows, int r, uint32_t* err) {
+  bool clipped = false;
+  const int64_t n = (int64_t)2 * rows * r;
+  for (int64_t o = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; o < n;
+       o += (int64_t)gridDim.x * blockDim.x) {
+    const int row = (int)(o / r), k = (int)(o % r);
+    const int qq = row / 128, rr = row % 128, g = rr / 32, up = (rr / 16) & 1, i = rr % 16;
+    const int src = qq * 64 + 16 * g + i;
+    const float v = __bfloat162float((up ? wu : wg)[(int64_t)src * r + k]);
+    clipped |= fabsf(v) > 65504.0f;
+    out[o] = __float2half_rn(fminf(fmaxf(v, -65504.0f), 65504.0f));
+  }
+  if (clipped) atomicOr(err, XP_ERR_RANGE);
+}
+}  // namespace
+
+cudaError_t xp_launch_gu_to_f16(const xp_head* h, const void* w_gate, const void* w_up,
+                                cudaStream_t s) {
+  const int64_t n = (int64_t)h->H * h->r;
+  gu_to_f16_kernel<<<(unsigned)std::min<int64_t>((2 * n + 255) / 256, 1024), 256, 0, s>>>(
+      (const bf16*)w_gate, (const bf16*)w_up, (__half*)h->wgu16, h->H, h->r, h->err);
+  return cudaGetLastError();
 }

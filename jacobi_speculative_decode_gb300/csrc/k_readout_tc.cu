@@ -15,7 +15,7 @@
 //
 // Warp roles (352 threads): warp 0 base producer, warp 1 MMA issuer (+ TMEM
 // owner), warp 2 w2 producer, warps 3..10 epilogue: warp w reads TMEM lane
-// group w % 4 and half (w - 3) / 4 of every 256-wide tile.
+// group w % 4 and half (w - 3) / 4 of every tile.
 #include <algorithm>
 
 #include "sm100_ptx.cuh"
@@ -29,12 +29,13 @@ constexpr int BM = 128;           // rows per MMA (TMEM lanes)
 constexpr int BN = 256;           // vocabulary ids per tile (MMA N)
 constexpr int BK = 64;            // k per swizzled chunk (128 bytes of bf16)
 constexpr int W2_STAGES = 3;      // k-chunks of w2 in flight (w2 is 2/3 of each SM's stream)
-constexpr int BASE_STAGES = 4;    // quarter tiles (64 ids) of base in flight
+constexpr int BASE_STAGES = 4;    // 64-id quarters of base in flight (one tile)
+constexpr int QPT = BN / 64;      // base quarters per tile
 constexpr int A_CHUNK_BYTES = BM * BK * 2;          // 16 KB
 constexpr int W2_STAGE_BYTES = BN * BK * 2;         // 32 KB
 constexpr int BASE_STAGE_BYTES = 128 * 64 * 2;      // 16 KB: one 64-wide box of <= 128 rows
 constexpr int NUM_THREADS = 352;   // 3 producer/MMA warps + 8 epilogue warps
-constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t TMEM_COLS = 2 * BN;   // double-buffered accumulator
 constexpr uint32_t IDESC = ptx::idesc_bf16_f32(BM, BN);
 
 struct Bars {
@@ -62,7 +63,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) readout_tc_kernel(
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
   uint8_t* sA = smem;                                    // KCH x 16 KB
   uint8_t* sW = sA + KCH * A_CHUNK_BYTES;                // W2_STAGES x 32 KB
-  uint8_t* sC = sW + W2_STAGES * W2_STAGE_BYTES;         // BASE_STAGES x 32 KB
+  uint8_t* sC = sW + W2_STAGES * W2_STAGE_BYTES;         // BASE_STAGES x 16 KB
   Bars* bars = reinterpret_cast<Bars*>(sC + BASE_STAGES * BASE_STAGE_BYTES);
   volatile int* abort = &bars->abort;
 
@@ -208,9 +209,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) readout_tc_kernel(
     }
   } else {
     // ---------------- epilogue: one row per thread, half of each tile per warp ----------------
-    static_assert(BASE_STAGES == BN / 64, "one base stage per quarter tile");
+    static_assert(QPT % 2 == 0 && BASE_STAGES % QPT == 0, "quarters split evenly");
     const int g = warp & 3;                  // TMEM lane group this warp may access
-    const int half = (warp - 3) >> 2;        // which 128 ids of every tile
+    const int half = (warp - 3) >> 2;        // which half of every tile's ids
     const int i = g * 32 + lane;             // row within the tile
     const uint32_t trow = tmem + ((uint32_t)(g * 32) << 16);
     float best = -INFINITY;
@@ -224,12 +225,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) readout_tc_kernel(
       if (!ok) break;
       ptx::tc_fence_after();
       const int vbase = vt * BN;
-      for (int qq = 0; qq < 2 && ok; ++qq) {
-        const int qt = half * 2 + qq;        // quarter tile == base ring stage
-        ok = ptx::mbar_wait(ptx::smem_u32(&bars->c_full[qt]), ti & 1, abort, err);
+      for (int qq = 0; qq < QPT / 2 && ok; ++qq) {
+        const int qt = half * (QPT / 2) + qq;              // quarter within the tile
+        const int ci = ti * QPT + qt, st = ci % BASE_STAGES;  // its slot in the base ring
+        ok = ptx::mbar_wait(ptx::smem_u32(&bars->c_full[st]), (ci / BASE_STAGES) & 1, abort, err);
         ok = __all_sync(0xFFFFFFFFu, ok);
         if (!ok) break;
-        const uint8_t* rowp = sC + qt * BASE_STAGE_BYTES + i * 128;
+        const uint8_t* rowp = sC + st * BASE_STAGE_BYTES + i * 128;
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
           const int col = qt * 64 + cc * 32;
@@ -268,7 +270,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) readout_tc_kernel(
           }
         }
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->c_empty[qt]));
+        if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->c_empty[st]));
       }
       ptx::tc_fence_before();
       __syncwarp();
@@ -336,6 +338,8 @@ cudaError_t launch(const xp_head* h, const CUtensorMap& tl, const CUtensorMap& t
 }
 
 }  // namespace
+
+int xp_readout_tc_tile() { return BN; }
 
 bool xp_readout_tc_call_ok(const xp_head* h, const void* lat, const void* base, int64_t sn,
                            int64_t sb, int N) {

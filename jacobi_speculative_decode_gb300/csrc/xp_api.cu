@@ -28,7 +28,7 @@ bool valid_weight_ptrs(const xp_weights* w) {
 }
 
 struct PrepLayout {
-  size_t err, w1, down_hg, w_hc, w_lat, mix, mixT, w_gate, w_up, w_down, w2, E, hfold, total;
+  size_t err, w1, down_hg, w_hc, w_lat, mix, mixT, w_gate, w_up, w_down, w2, E, hfold, wgu16, total;
 };
 
 PrepLayout prep_layout(const xp_weights* w) {
@@ -52,6 +52,7 @@ PrepLayout prep_layout(const xp_weights* w) {
   L.E = take(xp_latent_mma_ok(w->r, w->H, w->B, w->dtype) ? V * r * 4 : 0);
   // folded hidden-cache projection (hi and lo bf16 planes), only where the tcgen05 path runs
   L.hfold = take(xp_hidden_tc_ok(w->r, w->hidden, w->dtype) ? 2 * 2 * r * hid * 2 : 0);
+  L.wgu16 = take(xp_latent_mma_ok(w->r, w->H, w->B, w->dtype) ? 2 * H * r * 2 : 0);
   L.total = o;
   return L;
 }
@@ -80,6 +81,7 @@ xp_status copy_weights(xp_head* h, const xp_weights* w, cudaStream_t s) {
   cp(h->w_down, w->w_down, r * H * es);
   cp(h->w2, w->w2, V * r * es);
   if (e == cudaSuccess && h->latent_mma) e = xp_launch_embed_table(h, s);
+  if (e == cudaSuccess && h->latent_mma) e = xp_launch_gu_to_f16(h, w->w_gate, w->w_up, s);
   if (e == cudaSuccess && h->hidden_tc) e = xp_launch_hidden_fold(h, w->in_proj, s);
   return e == cudaSuccess ? XP_OK : XP_ECUDA;
 }
@@ -132,6 +134,7 @@ const char* xp_status_str(xp_status s) {
     case XP_EBADTOKEN: return "token id out of range (clamped)";
     case XP_ETIMEOUT: return "bounded wait in a kernel timed out";
     case XP_EUNSUPPORTED: return "unsupported shape";
+    case XP_ERANGE: return "latent value outside the fp16 exchange range (saturated)";
   }
   return "unknown status";
 }
@@ -181,10 +184,12 @@ xp_status xp_head_create(const xp_weights* w, void* prep_dev, size_t prep_bytes,
   h->mixT = p + L.mixT;
   h->E = (float*)(p + L.E);
   h->hfold = p + L.hfold;
+  h->wgu16 = p + L.wgu16;
   h->w_gate = p + L.w_gate; h->w_up = p + L.w_up; h->w_down = p + L.w_down; h->w2 = p + L.w2;
   decide_paths(h);
-  xp_status st = copy_weights(h, w, stream);
-  if (st == XP_OK) st = cuda_status(cudaMemsetAsync(h->err, 0, 256, stream));
+  // the error word starts clear; the weight preparation below may already flag it
+  xp_status st = cuda_status(cudaMemsetAsync(h->err, 0, 256, stream));
+  if (st == XP_OK) st = copy_weights(h, w, stream);
   if (st != XP_OK) { delete h; return st; }
   *out = h;
   return XP_OK;
@@ -226,7 +231,9 @@ xp_status xp_latent_pass(const xp_head* h, const int64_t* blk, const int64_t* am
   if (!blk || !am1 || !xh || !lat || N < 0) return XP_EINVAL;
   if (N > h->max_N) return XP_ECAPACITY;
   if (N == 0) return XP_OK;
-  if (h->latent_mma) return cuda_status(xp_launch_latent_mma(h, blk, am1, xh, N, lat, stream));
+  // the tensor-core latent reads xh in 16-byte pieces and writes lat in channel pairs
+  if (h->latent_mma && (uintptr_t)xh % 16 == 0 && (uintptr_t)lat % 4 == 0)
+    return cuda_status(xp_launch_latent_mma(h, blk, am1, xh, N, lat, stream));
   return cuda_status(xp_launch_latent_simt(h, blk, am1, xh, N, lat, stream));
 }
 
@@ -341,6 +348,7 @@ xp_status xp_get_error(const xp_head* h, cudaStream_t stream) {
     return XP_ECUDA;
   if (cudaMemset(h->err, 0, sizeof(word)) != cudaSuccess) return XP_ECUDA;
   if (word & XP_ERR_TIMEOUT) return XP_ETIMEOUT;
+  if (word & XP_ERR_RANGE) return XP_ERANGE;
   if (word & XP_ERR_BADTOKEN) return XP_EBADTOKEN;
   return XP_OK;
 }
@@ -385,7 +393,7 @@ static void decide_paths(xp_head* h) {
     CUtensorMap tm;
     const cuuint64_t dims[2] = {(cuuint64_t)h->r, (cuuint64_t)h->V};
     const cuuint64_t strides[1] = {(cuuint64_t)h->r * 2};
-    const cuuint32_t box[2] = {64, 256};
+    const cuuint32_t box[2] = {64, (cuuint32_t)xp_readout_tc_tile()};
     const cuuint32_t es[2] = {1, 1};
     if (xp_get_encode_tiled()(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, h->w2, dims, strides, box,
                               es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

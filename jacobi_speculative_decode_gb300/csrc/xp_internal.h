@@ -17,6 +17,7 @@ struct xp_head {
   size_t prep_bytes;
   uint32_t* err;         // device error word (XP_ERR_* bits)
   void *w1, *down_hg, *w_hc, *w_lat, *mix, *w_gate, *w_up, *w_down, *w2;  // down_hg = [down_h ; down_g]
+  void* wgu16;           // [w_gate ; w_up] as fp16 in cluster row order (tensor-core latent only)
   void* mixT;            // folded mixer laid out [out slot][in slot][channel]
   float* E;              // w1 . in_proj[:, 2r:]^T, fp32 [V, r] (tensor-core latent only)
   void* hfold;           // [in_proj[:, :r] . down_h ; in_proj[:, r:2r] . down_g] as bf16 hi, lo planes
@@ -25,11 +26,11 @@ struct xp_head {
   int readout_tc;        // tcgen05 readout usable for this head's shapes
   int latent_mma;        // cluster tensor-core latent usable for this head's shapes
   CUtensorMap tm_w2;     // W2 [V, r] tiled map for the tcgen05 readout
-  CUtensorMap tm_wg, tm_wu, tm_wd, tm_mixT;   // latent weight / mixer slices (TMA)
+  CUtensorMap tm_wgu, tm_wd, tm_mixT;  // [w_gate ; w_up] fp16 rows, w_down, mixer slices (TMA)
 };
 
 // device error word bits
-enum : uint32_t { XP_ERR_BADTOKEN = 1u, XP_ERR_TIMEOUT = 2u };
+enum : uint32_t { XP_ERR_BADTOKEN = 1u, XP_ERR_TIMEOUT = 2u, XP_ERR_RANGE = 4u };
 
 // Workspace layout.  Regions that must stay zero between calls come first and
 // are sized by the head's max_N so that the layout never moves with N.
@@ -73,6 +74,9 @@ cudaError_t xp_launch_latent_simt(const xp_head* h, const int64_t* blk, const in
                                   const float* xh, int N, void* lat, cudaStream_t s);
 bool xp_latent_mma_ok(int r, int H, int B, xp_dtype dt);
 bool xp_latent_mma_maps(xp_head* h);
+// w_gate / w_up copied to fp16 for the tensor-core latent (saturating; XP_ERR_RANGE)
+cudaError_t xp_launch_gu_to_f16(const xp_head* h, const void* w_gate, const void* w_up,
+                                cudaStream_t s);
 cudaError_t xp_launch_latent_mma(const xp_head* h, const int64_t* blk, const int64_t* am1,
                                  const float* xh, int N, void* lat, cudaStream_t s);
 
@@ -83,6 +87,7 @@ cudaError_t xp_launch_readout_simt(const xp_head* h, const void* lat, const void
 cudaError_t xp_launch_readout_tc(const xp_head* h, const void* lat, const void* base,
                                  int64_t sn, int64_t sb, int N, int64_t* blk, float* win,
                                  unsigned long long* packed, unsigned* ticket, cudaStream_t s);
+int xp_readout_tc_tile();   // vocabulary ids per tile of the tcgen05 readout (w2 map box rows)
 bool xp_readout_tc_call_ok(const xp_head* h, const void* lat, const void* base, int64_t sn,
                            int64_t sb, int N);
 

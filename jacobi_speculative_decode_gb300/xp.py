@@ -17,9 +17,9 @@ LIB_PATH = os.path.join(_HERE, "libxp.so")
 
 XP_BF16, XP_F32 = 0, 1
 STATUS = {0: "XP_OK", 1: "XP_EINVAL", 2: "XP_ECAPACITY", 3: "XP_ENOTPREPARED", 4: "XP_ECUDA",
-          5: "XP_EBADTOKEN", 6: "XP_ETIMEOUT", 7: "XP_EUNSUPPORTED"}
+          5: "XP_EBADTOKEN", 6: "XP_ETIMEOUT", 7: "XP_EUNSUPPORTED", 8: "XP_ERANGE"}
 XP_OK, XP_EINVAL, XP_ECAPACITY, XP_ENOTPREPARED, XP_ECUDA, XP_EBADTOKEN, XP_ETIMEOUT, \
-    XP_EUNSUPPORTED = range(8)
+    XP_EUNSUPPORTED, XP_ERANGE = range(9)
 
 
 class XPError(RuntimeError):

@@ -37,7 +37,7 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for code in range(8):
+    for code in range(9):
         assert xp.status_str(code) and xp.status_str(code) != "unknown status"
 
 
@@ -53,9 +53,11 @@ def test_sizes(lib):
     prep = xp.xp_head_prep_bytes(w)
     # every prepared copy is present: w1 + w2 + down_h + down_g + in_proj + mix + MLP,
     # plus the [b][j][channel] copy of the mixer, the fp32 projected embedding table and
-    # the folded hidden-cache projection [2r, hidden] as two bf16 planes (hi, lo)
+    # the folded hidden-cache projection [2r, hidden] as two bf16 planes (hi, lo) and
+    # the fp16 copies of the SwiGLU input weights
     floor = es * (2 * 151936 * 256 + 2 * 256 * 4096 + 3 * 256 * 256 + 256 * 16 * 16 + 3 * 512 * 256)
     floor += es * 256 * 16 * 16 + 4 * 151936 * 256 + 2 * es * 512 * 4096
+    floor += 2 * 2 * 512 * 256      # fp16 copies of w_gate and w_up
     assert floor <= prep <= floor + 64 * 1024
     ws0 = xp.xp_workspace_bytes(w, 32, 0)
     ws1 = xp.xp_workspace_bytes(w, 32, 512)

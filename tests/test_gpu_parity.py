@@ -300,3 +300,49 @@ def test_latent_persistent_many_groups():
     want = O.latent(d["blk"], d["am1"], xh_np.astype(np.float64), p)
     check_close(O.decode(xp.to_host_storage(lat), "bf16"), want, LAT_TOL["bf16"], "lat")
     dev.close()
+
+
+def test_fp16_range_flag():
+    # the tensor-core latent exchanges fp16: a weight or a latent value past its range
+    # saturates and is reported, never silently turned into inf
+    wl = I.workload("batched-decode", V=4096, hidden=64, N=4, K=1)
+    d = I.make_inputs(wl)
+    d["w_gate"] = d["w_gate"].copy()
+    d["w_gate"][3, 5] = I.f32_to_bf16_bits(np.float32([1.0e6]))[0]
+    dev = Dev(d, wl)
+    assert xp.xp_get_error(dev.head.handle) == xp.XP_ERANGE
+    dev.close()
+    d = I.make_inputs(wl)
+    dev = Dev(d, wl)
+    assert xp.xp_get_error(dev.head.handle) == xp.XP_OK
+    xh_np = I.random_xh(wl, seed=3)
+    xh_np[1, 2, 7] = 1.0e6
+    lat = torch.empty(wl.N, wl.B - 1, wl.r, dtype=torch.bfloat16, device="cuda")
+    xp.xp_latent_pass(dev.head.handle, dev.blk_in, dev.am1, torch.from_numpy(xh_np).cuda(), wl.N,
+                      lat)
+    assert xp.xp_get_error(dev.head.handle) == xp.XP_ERANGE
+    dev.close()
+
+
+@pytest.mark.parametrize("B,N", [(3, 37), (32, 5), (7, 41)])
+def test_latent_group_shapes(B, N):
+    # blocks per row group of the cluster latent: 10 (generic path), 1 and 4 / 6
+    wl = I.workload("batched-decode", V=4096, hidden=64, B=B, N=N, K=2)
+    d = I.make_inputs(wl)
+    dev = Dev(d, wl)
+    p = O.params_from_inputs(d, wl.dtype)
+    xh_np = I.random_xh(wl, seed=11)
+    lat = torch.empty(wl.N, wl.B - 1, wl.r, dtype=torch.bfloat16, device="cuda")
+    xp.xp_latent_pass(dev.head.handle, dev.blk_in, dev.am1, torch.from_numpy(xh_np).cuda(), wl.N,
+                      lat)
+    assert xp.xp_get_error(dev.head.handle) == xp.XP_OK
+    want = O.latent(d["blk"], d["am1"], xh_np.astype(np.float64), p)
+    check_close(O.decode(xp.to_host_storage(lat), "bf16"), want, LAT_TOL["bf16"], "lat")
+    blk = torch.full((wl.N, wl.B), -1, dtype=torch.int64, device="cuda")
+    xp.xp_jacobi_refine(dev.head.handle, dev.base, dev.sn, dev.sb, dev.h, dev.anchor, dev.am1,
+                        wl.N, wl.K, 0, blk, dev.ws)
+    assert xp.xp_get_error(dev.head.handle) == xp.XP_OK
+    want_blk, margins = O.jacobi_refine(O.decode(d["base"], "bf16"), O.decode(d["h_full"], "bf16"),
+                                        d["anchor"], d["am1"], wl.K, p)
+    check_blocks(blk.cpu().numpy(), want_blk, margins, f"jacobi B={B}")
+    dev.close()
