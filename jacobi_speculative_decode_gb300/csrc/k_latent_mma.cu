@@ -19,20 +19,21 @@
 //   3. [gate ; up] = [w_gate ; w_up][own units] u^T, tcgen05.mma kind::f16 on fp16
 //      operands (the head keeps fp16 copies of w_gate and w_up), the weights as the
 //      M = 128 side and the group's rows as N = MT; the weight rows are interleaved
-//      so that one TMEM lane quadrant holds gate and up of the same 16 units; as soon
-//      as the MMAs retire, w_down's column slice for the own units streams by TMA
-//      into the u buffer; a = silu(gate) * up as bf16 hi + lo
+//      so that one TMEM lane quadrant holds gate and up of the same 16 units;
+//      a = silu(gate) * up as bf16 hi + lo
 //   4. partial = w_down[:, own units] a^T for ALL r channels (two M = 128 tiles, the
 //      activations' hi rows and lo rows side by side as N = 2*MT, summed when read
-//      back), staged by the warp whose lanes hold owner p's channels as
-//      [channel][row pair] fp16 and sent to owner p with one bulk copy
+//      back; w_down's slice stays resident), staged by the warp whose lanes hold
+//      owner p's channels as [channel][row pair] fp16 and sent by that warp to owner
+//      p with one bulk copy
 //   5. lat = u + the 8 partials of the own channels, added in a fixed order (fp32)
 // The fp16 exchanges halve the bytes that cross the cluster network, whose
 // bandwidth per SM sets their latency; fp16's 2^-11 relative error is a quarter of
 // the bf16 rounding of the stored latent.  Values beyond the fp16 range saturate
 // and raise XP_ERR_RANGE.
 // The only cluster-wide barrier per group is a split arrive/wait that keeps a
-// CTA from sending into buffers a peer is still reading; after its last group a
+// CTA from sending into buffers a peer is still reading; the first one (barriers
+// initialised) is waited on just before the first send, and after its last group a
 // CTA arrives as soon as everything addressed to it has landed.
 //
 // Shared-memory operand layouts (what the TMA writes and tcgen05 reads):
@@ -65,7 +66,7 @@ __host__ __device__ constexpr int blk_bytes(int MT) { return ((CS * (MT / 2 + 1)
 
 struct Plan {                  // byte offsets into dynamic shared memory
   int MT;
-  int wgu, mix, ubuf, uout, act, rcv, sx, us, rowi, bars;
+  int wgu, wd, mix, ubuf, uout, act, rcv, sx, us, rowi, bars;
   int mix_rows;
   int total;
 };
@@ -84,17 +85,17 @@ __host__ __device__ inline Plan make_plan(int MT, int B) {
     return at;
   };
   p.wgu = take((R / 64) * 128 * 128, 1024);     // own w_gate / w_up rows (interleaved), 128B swizzle
+  p.wd = take(R * HS * 2, 1024);                // w_down[:, own units], R rows x 64, 128B swizzle
   p.mix = take(mparts * mbox * CS * 2, 1024);
-  // u (fp16) of the 8 senders (64B swizzle), later w_down[:, own] (R rows x 64, 128B
-  // swizzle), later the 7 outgoing partial blocks
-  p.ubuf = take(std::max(std::max(CL * MT * 64, R * HS * 2), (CL - 1) * blk_bytes(MT)), 1024);
+  // u (fp16) of the 8 senders (64B swizzle), later the 7 outgoing partial blocks
+  p.ubuf = take(std::max(CL * MT * 64, (CL - 1) * blk_bytes(MT)), 1024);
   p.uout = take(MT * 64, 1024);                 // own u: the MMA's and the peers' copy
   p.act = take(2 * MT * 128, 1024);             // activations hi rows then lo rows, 64 units, 128B swizzle
   p.rcv = take(CL * blk_bytes(MT), 16);         // partial blocks by sender (own one at slot q)
   p.sx = take(MT * CS * 4, 16);                 // x = xh + E[prev], own channels
   p.us = take(MT * CS * 4, 16);                 // u fp32, own channels (the residual)
   p.rowi = take(MT * 4, 16);                    // lat row of each group row, -1 = not stored
-  p.bars = take(64, 16);
+  p.bars = take(64, 16);                        // 4 mbarriers + the TMEM address
   p.total = o;
   return p;
 }
@@ -144,8 +145,9 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
 __device__ __forceinline__ void cluster_arrive() {
   asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 }
-// arrive without ordering this thread's earlier memory operations (exit protocol only:
-// every byte addressed to this CTA was already observed through its mbarriers)
+// arrive without ordering this thread's earlier memory operations: used where what
+// the peers need was already published (mbarrier inits by fence.mbarrier_init, or
+// every byte addressed to this CTA observed through its mbarriers before exit)
 __device__ __forceinline__ void cluster_arrive_relaxed() {
   asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 }
@@ -268,50 +270,52 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1) latent_
   float* sUs = (float*)(sm + P.us);
   int* sRow = (int*)(sm + P.rowi);
   const uint32_t* sRcv = (const uint32_t*)(sm + P.rcv);
-  const uint32_t bar_w = s0 + P.bars, bar_wd = bar_w + 8, bar_u = bar_w + 16, bar_p = bar_w + 24;
-  const uint32_t bar_mma = bar_w + 32;
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + P.bars + 40);
+  const uint32_t bar_w = s0 + P.bars, bar_u = bar_w + 8, bar_p = bar_w + 16;
+  const uint32_t bar_mma = bar_w + 24;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + P.bars + 32);
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   const int nb = MT / B;                   // blocks per group
   const int groups = (N + nb - 1) / nb;
-  const uint32_t u_bytes_in = (uint32_t)((CL - 1) * SLICE);
   const uint32_t p_bytes_in = (uint32_t)((CL - 1) * BLK);
   const uint64_t pol = ptx::policy_evict_last();
 
-  // ---- set-up: barriers, the resident weight and mixer slices by TMA (one box per
-  // lane of warp 0), TMEM (warp 1) ----
+  // ---- set-up: barriers, the resident weight and mixer slices by TMA (warp 0), TMEM
+  // (warp 1); the cluster barrier that lets peers send here is waited on only just
+  // before this CTA's first send, so its latency hides behind the first gather ----
   if (warp == 0) {
     if (lane == 0) {
       ptx::mbar_init(bar_w, 1);
-      ptx::mbar_init(bar_wd, 1);
-      ptx::mbar_init(bar_u, 1);
       ptx::mbar_init(bar_p, 1);
       ptx::mbar_init(bar_mma, 1);
+      ptx::mbar_init(bar_u, 1);
       ptx::fence_barrier_init();
       const int mparts = (P.mix_rows + 255) / 256, mbox = std::min(P.mix_rows, 256);
-      ptx::mbar_arrive_expect_tx(bar_w, 2 * HS * R * 2 + mparts * mbox * CS * 2);
+      ptx::mbar_arrive_expect_tx(bar_w, 2 * HS * R * 2 + R * HS * 2 + mparts * mbox * CS * 2);
       for (int pt = 0; pt < mparts; ++pt)
         ptx::tma_load_2d(s0 + P.mix + pt * mbox * CS * 2, &maps.mix, bar_w, q * CS, pt * mbox,
                          pol);
       // the first group's incoming u and partial blocks
-      ptx::mbar_arrive_expect_tx(bar_u, u_bytes_in);
+      ptx::mbar_arrive_expect_tx(bar_u, (CL - 1) * SLICE);
       ptx::mbar_arrive_expect_tx(bar_p, p_bytes_in);
     }
     __syncwarp();
     // the head keeps [w_gate ; w_up] in this CTA's row order (see xp_launch_gu_to_f16):
-    // one 128-row box per 64-wide k chunk
+    // one 128-row box per 64-wide k chunk; w_down's column slice in one box
     if (lane < R / 64)
       ptx::tma_load_2d(aW + lane * 16384, &maps.wgu, bar_w, lane * 64, q * 128, pol);
+    else if (lane == R / 64)
+      ptx::tma_load_2d(s0 + P.wd, &maps.wdk, bar_w, q * HS, 0, pol);
   } else if (warp == 1) {
     ptx::tmem_alloc(ptx::smem_u32(s_tmem), TMEM_COLS);
     ptx::tmem_relinquish();
   }
-  // peers send into this CTA only after its barriers exist
   ptx::tc_fence_before();
-  cluster_arrive();
+  // this CTA's barriers exist (fence.mbarrier_init above published them to the cluster,
+  // so the arrive needs no release of its own)
+  cluster_arrive_relaxed();
   ptx::pdl_wait();                         // blk (and xh) come from earlier kernels
   ptx::pdl_trigger();
-  cluster_wait();
+  __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *s_tmem;
   {
@@ -391,6 +395,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1) latent_
     }
     fence_async_smem();                    // the bulk copies and the MMA read u
     __syncthreads();
+    if (it == 0) cluster_wait();           // the set-up arrive: every peer's barriers exist
     if (tid == 0) {
       for (int dp = 1; dp < CL; ++dp) {
         const int p = (q + dp) % CL;
@@ -399,7 +404,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1) latent_
     }
     mbar_wait_cluster(bar_u, ph, err);
 
-    // ---- 3. [gate ; up] (units x rows) from u = hi + lo; w_down streams in behind ----
+    // ---- 3. [gate ; up] (units x rows) ----
     if (tid == 0) {
       ptx::tc_fence_after();
       constexpr uint32_t ID = ptx::idesc_f16_f32(128, MT);
@@ -412,12 +417,8 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1) latent_
         ptx::mma_bf16(tmem + COL_GU, dw + (((s / 4) * 16384 + (s % 4) * 32) >> 4), bd, ID, s != 0);
       }
       ptx::mma_commit(bar_mma);
-      volatile int no_abort = 0;
-      ptx::mbar_wait(bar_mma, mma_phase, &no_abort, err);
-      // u is dead: w_down's column slice for the own units goes into its buffer
-      ptx::mbar_arrive_expect_tx(bar_wd, R * HS * 2);
-      ptx::tma_load_2d(aU, &maps.wdk, bar_wd, q * HS, 0, pol);
-    } else {
+    }
+    {
       volatile int no_abort = 0;
       ptx::mbar_wait(bar_mma, mma_phase, &no_abort, err);
     }
@@ -451,11 +452,9 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1) latent_
 
     // ---- 4. partial down projection over own units, channels x rows (two M tiles) ----
     if (tid == 0) {
-      volatile int no_abort = 0;
-      ptx::mbar_wait(bar_wd, ph, &no_abort, err);
       ptx::tc_fence_after();
       constexpr uint32_t ID = ptx::idesc_bf16_f32(128, 2 * MT);
-      const uint64_t dw = ptx::sw128_desc(aU), da = ptx::sw128_desc(aAct);
+      const uint64_t dw = ptx::sw128_desc(s0 + P.wd), da = ptx::sw128_desc(aAct);
 #pragma unroll
       for (int t = 0; t < R / 128; ++t)
 #pragma unroll
@@ -490,17 +489,16 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1) latent_
         }
       }
       if (out_of_range) atomicOr(err, XP_ERR_RANGE);
-    }
-    ptx::tc_fence_before();
-    fence_async_smem();                    // the bulk copies read the staged blocks
-    __syncthreads();
-    if (tid == 0) {
-      for (int dp = 1; dp < CL; ++dp) {
-        const int p = (q + dp) % CL;
-        ptx::bulk_copy_to_peer(mapa(s0 + P.rcv + q * BLK, p), aU + (dp - 1) * BLK, BLK,
-                               mapa(bar_p, p));
+      if (p != q) {                        // the warp sends its block as soon as it is staged
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0)
+          ptx::bulk_copy_to_peer(mapa(s0 + P.rcv + q * BLK, p), ptx::smem_u32(dst), BLK,
+                                 mapa(bar_p, p));
       }
     }
+    ptx::tc_fence_before();
+    __syncthreads();                       // the own block is visible to the sum
     mbar_wait_cluster(bar_p, ph, err);
     // everything addressed to this CTA has landed: after its last group it can
     // release the peers' exit barrier now
@@ -524,9 +522,9 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1) latent_
     if (!last) {
       __syncthreads();
       // arm the next group's receive barriers, then tell the peers this CTA's
-      // buffers (u, w_down slice, staged and received partials) are free again
+      // buffers (u, staged and received partials) are free again
       if (tid == 0) {
-        ptx::mbar_arrive_expect_tx(bar_u, u_bytes_in);
+        ptx::mbar_arrive_expect_tx(bar_u, (CL - 1) * SLICE);
         ptx::mbar_arrive_expect_tx(bar_p, p_bytes_in);
       }
       cluster_arrive();

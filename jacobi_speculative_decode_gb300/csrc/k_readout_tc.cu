@@ -57,6 +57,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) readout_tc_kernel(
     const __grid_constant__ CUtensorMap tm_lat, const __grid_constant__ CUtensorMap tm_w2,
     const __grid_constant__ CUtensorMap tm_base, int rows, int Bm1, int B, int V, int rpt, int bpt,
     int n_rt, int n_seg, int nvt, int64_t* __restrict__ blk, float* __restrict__ win,
+    const float* __restrict__ pf_rows, int pf_row_bytes,
     unsigned long long* __restrict__ packed, unsigned* __restrict__ ticket, uint32_t* err) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = ptx::smem_u32(smem_raw);
@@ -289,8 +290,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) readout_tc_kernel(
     if (threadIdx.x < rpt && grow < rows) {
       const unsigned long long pk = atomicExch(packed + grow, 0ull);
       const int n = grow / Bm1, b = grow % Bm1;
-      blk[(int64_t)n * B + 1 + b] = (int64_t)packed_idx(pk);
+      const uint32_t id = packed_idx(pk);
+      blk[(int64_t)n * B + 1 + b] = (int64_t)id;
       if (win) win[grow] = packed_val(pk);
+      // the next latent stage gathers the row of pf_rows this token selects: ask L2 for
+      // it now, while the other row tiles finish
+      if (pf_rows) {
+        const char* rp = reinterpret_cast<const char*>(pf_rows) + (int64_t)id * pf_row_bytes;
+        for (int o = 0; o < pf_row_bytes; o += 128)
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(rp + o));
+      }
     }
     if (threadIdx.x == 0) ticket[tile] = 0u;
   }
@@ -333,6 +342,7 @@ cudaError_t launch(const xp_head* h, const CUtensorMap& tl, const CUtensorMap& t
   if (e != cudaSuccess) return e;
   e = xp_launch_pdl(readout_tc_kernel<KCH>, dim3(n_rt * n_seg), dim3(NUM_THREADS), smem, s, tl,
                     h->tm_w2, tb, rows, Bm1, h->B, h->V, rpt, bpt, n_rt, n_seg, nvt, blk, win,
+                    h->latent_mma ? (const float*)h->E : (const float*)nullptr, h->r * 4,
                     packed, ticket, h->err);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
