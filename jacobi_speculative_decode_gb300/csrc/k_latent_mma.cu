@@ -95,7 +95,7 @@ __host__ __device__ inline Plan make_plan(int MT, int B) {
   p.sx = take(MT * CS * 4, 16);                 // x = xh + E[prev], own channels
   p.us = take(MT * CS * 4, 16);                 // u fp32, own channels (the residual)
   p.rowi = take(MT * 4, 16);                    // lat row of each group row, -1 = not stored
-  p.bars = take(64, 16);                        // 4 mbarriers + the TMEM address
+  p.bars = take(64, 16);                        // 5 mbarriers + the TMEM address
   p.total = o;
   return p;
 }
@@ -270,9 +270,10 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1) latent_
   float* sUs = (float*)(sm + P.us);
   int* sRow = (int*)(sm + P.rowi);
   const uint32_t* sRcv = (const uint32_t*)(sm + P.rcv);
+  // bar_mix: the mixer slice; bar_w: the weight slices (needed first by the MMAs)
   const uint32_t bar_w = s0 + P.bars, bar_u = bar_w + 8, bar_p = bar_w + 16;
-  const uint32_t bar_mma = bar_w + 24;
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + P.bars + 32);
+  const uint32_t bar_mma = bar_w + 24, bar_mix = bar_w + 32;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + P.bars + 40);
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   const int nb = MT / B;                   // blocks per group
   const int groups = (N + nb - 1) / nb;
@@ -288,12 +289,14 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1) latent_
       ptx::mbar_init(bar_p, 1);
       ptx::mbar_init(bar_mma, 1);
       ptx::mbar_init(bar_u, 1);
+      ptx::mbar_init(bar_mix, 1);
       ptx::fence_barrier_init();
       const int mparts = (P.mix_rows + 255) / 256, mbox = std::min(P.mix_rows, 256);
-      ptx::mbar_arrive_expect_tx(bar_w, 2 * HS * R * 2 + R * HS * 2 + mparts * mbox * CS * 2);
+      ptx::mbar_arrive_expect_tx(bar_mix, mparts * mbox * CS * 2);
       for (int pt = 0; pt < mparts; ++pt)
-        ptx::tma_load_2d(s0 + P.mix + pt * mbox * CS * 2, &maps.mix, bar_w, q * CS, pt * mbox,
+        ptx::tma_load_2d(s0 + P.mix + pt * mbox * CS * 2, &maps.mix, bar_mix, q * CS, pt * mbox,
                          pol);
+      ptx::mbar_arrive_expect_tx(bar_w, 2 * HS * R * 2 + R * HS * 2);
       // the first group's incoming u and partial blocks
       ptx::mbar_arrive_expect_tx(bar_u, (CL - 1) * SLICE);
       ptx::mbar_arrive_expect_tx(bar_p, p_bytes_in);
@@ -318,10 +321,6 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1) latent_
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *s_tmem;
-  {
-    volatile int no_abort = 0;
-    ptx::mbar_wait(bar_w, 0, &no_abort, err);
-  }
   uint32_t mma_phase = 0;
   const int quad = warp & 3, half = warp >> 2;
 
@@ -372,6 +371,10 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1) latent_
     if (it > 0) cluster_wait();
 
     // ---- 2. u = per-channel causal mix (fp32): item = (slot b, channel pair) ----
+    if (it == 0) {
+      volatile int no_abort = 0;
+      ptx::mbar_wait(bar_mix, 0, &no_abort, err);
+    }
     {
       uint8_t* uh = sm + P.uout;                     // own u (fp16)
       bool out_of_range = false;
@@ -406,6 +409,10 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1) latent_
 
     // ---- 3. [gate ; up] (units x rows) ----
     if (tid == 0) {
+      if (it == 0) {
+        volatile int no_abort = 0;
+        ptx::mbar_wait(bar_w, 0, &no_abort, err);
+      }
       ptx::tc_fence_after();
       constexpr uint32_t ID = ptx::idesc_f16_f32(128, MT);
       const uint64_t dw = ptx::sw128_desc(aW), du = ptx::sw64_desc(aU);

@@ -378,6 +378,7 @@ xp_encode_tiled_fn xp_get_encode_tiled() {
 
 static void decide_paths(xp_head* h) {
   h->readout_tc = 0;
+  h->readout_mc = 0;
   h->latent_mma = 0;
   h->hidden_tc = 0;
   int major = 0, minor = 0;
@@ -401,6 +402,16 @@ static void decide_paths(xp_head* h) {
                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS) {
       h->tm_w2 = tm;
       h->readout_tc = 1;
+      // the same map with half and quarter boxes, for the cluster-multicast readout
+      h->readout_mc = 1;
+      for (int i = 0; i < 2 && h->readout_mc; ++i) {
+        const cuuint32_t sbox[2] = {64, (cuuint32_t)(xp_readout_tc_tile() >> (i + 1))};
+        h->readout_mc =
+            xp_get_encode_tiled()(&h->tm_w2_slice[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, h->w2,
+                                  dims, strides, sbox, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+      }
     }
   }
 }

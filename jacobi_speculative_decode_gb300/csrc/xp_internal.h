@@ -26,6 +26,8 @@ struct xp_head {
   int readout_tc;        // tcgen05 readout usable for this head's shapes
   int latent_mma;        // cluster tensor-core latent usable for this head's shapes
   CUtensorMap tm_w2;     // W2 [V, r] tiled map for the tcgen05 readout
+  CUtensorMap tm_w2_slice[2];  // the same with 1/2 and 1/4 of the tile's rows (multicast slices)
+  int readout_mc;        // cluster-multicast readout variants usable
   CUtensorMap tm_wgu, tm_wd, tm_mixT;  // [w_gate ; w_up] fp16 rows, w_down, mixer slices (TMA)
 };
 
