@@ -15,8 +15,9 @@
 //
 // GEMM CTA (192 threads): warp 0 TMA producer, warp 1 TMEM owner + MMA issuer,
 // warps 2..5 epilogue (warp w reads TMEM lanes 32*(w%4)..+31).  Tile 128 rows x
-// 256 output columns, k-chunks of 64 (128-byte swizzled), 2-stage ring of
-// {h chunk 16 KB, hi chunk 32 KB, lo chunk 32 KB}.
+// 128 output columns, k-chunks of 64 (128-byte swizzled), 4-stage ring of
+// {h chunk 16 KB, hi chunk 16 KB, lo chunk 16 KB}; the K range is split over
+// about one CTA per SM.
 #include <algorithm>
 
 #include "sm100_ptx.cuh"
@@ -27,14 +28,14 @@ typedef __nv_bfloat16 bf16;
 namespace {
 
 constexpr int HM = 128;                 // rows per tile (TMEM lanes)
-constexpr int HN = 256;                 // output columns per tile (MMA N)
+constexpr int HN = 128;                 // output columns per tile (MMA N)
 constexpr int HK = 64;                  // k per swizzled chunk
-constexpr int STAGES = 2;
+constexpr int STAGES = 4;
 constexpr int A_BYTES = HM * HK * 2;    // 16 KB
-constexpr int B_BYTES = HN * HK * 2;    // 32 KB
+constexpr int B_BYTES = HN * HK * 2;    // 16 KB
 constexpr int STAGE_BYTES = A_BYTES + 2 * B_BYTES;
 constexpr int THREADS = 192;
-constexpr uint32_t TMEM_COLS = 256;
+constexpr uint32_t TMEM_COLS = HN;
 constexpr uint32_t IDESC = ptx::idesc_bf16_f32(HM, HN);
 constexpr int MAX_SPLITS = 64;
 
@@ -205,7 +206,8 @@ __global__ void __launch_bounds__(256) xh_reduce_kernel(const float* __restrict_
   if (c < r)
     for (int b = ty; b < B; b += 8) {
       const float* p = P + ((int64_t)n * B + b) * two_r + r + c;
-      for (int zz = 0; zz < splits; ++zz) gsum += p[zz * split_stride];
+#pragma unroll 8
+      for (int zz = 0; zz < splits; ++zz) gsum += __ldg(p + zz * split_stride);
     }
   red[ty][tx] = gsum;
   __syncthreads();
@@ -218,7 +220,8 @@ __global__ void __launch_bounds__(256) xh_reduce_kernel(const float* __restrict_
       const int64_t row = (int64_t)n * B + b;
       const float* p = P + row * two_r + c;
       float s = 0.f;
-      for (int zz = 0; zz < splits; ++zz) s += p[zz * split_stride];
+#pragma unroll 8
+      for (int zz = 0; zz < splits; ++zz) s += __ldg(p + zz * split_stride);
       xh[row * r + c] = s + mean;
     }
 }
@@ -241,7 +244,7 @@ constexpr size_t kSmem = 1024 + (size_t)STAGES * STAGE_BYTES + sizeof(Bars);
 }  // namespace
 
 bool xp_hidden_tc_ok(int r, int hidden, xp_dtype dt) {
-  return dt == XP_BF16 && (2 * r) % HN == 0 && hidden % 8 == 0 && r % 4 == 0;
+  return dt == XP_BF16 && (2 * r) % HN == 0 && hidden % 8 == 0;
 }
 
 bool xp_hidden_tc_map(xp_head* h) {
