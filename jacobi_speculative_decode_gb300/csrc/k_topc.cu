@@ -22,6 +22,27 @@ __device__ __forceinline__ uint32_t radix_key(bf16 x) {
 }
 __device__ __forceinline__ uint32_t radix_key(float x) { return f2key(x); }
 
+// the value a radix key stands for (+0 for the shared key of -0 and +0)
+__device__ __forceinline__ float key_value(uint32_t k, bf16*) {
+  const uint32_t u = (k & 0x8000u) ? (k & 0x7FFFu) : (~k & 0xFFFFu);
+  return __uint_as_float(u << 16);
+}
+__device__ __forceinline__ float key_value(uint32_t k, float*) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+// largest of 8 values (packed bf16 pairs for bf16)
+__device__ __forceinline__ float max8(const bf16 (&x)[8]) {
+  const __nv_bfloat162* v = reinterpret_cast<const __nv_bfloat162*>(x);
+  const __nv_bfloat162 m = __hmax2(__hmax2(v[0], v[1]), __hmax2(v[2], v[3]));
+  return fmaxf(__low2float(m), __high2float(m));
+}
+__device__ __forceinline__ float max8(const float (&x)[8]) {
+  float m = x[0];
+#pragma unroll
+  for (int i = 1; i < 8; ++i) m = fmaxf(m, x[i]);
+  return m;
+}
+
 template <typename T> struct KeyBits;
 template <> struct KeyBits<bf16> { static constexpr int value = 16; };
 template <> struct KeyBits<float> { static constexpr int value = 32; };
@@ -52,103 +73,294 @@ __device__ __forceinline__ uint32_t block_incl_scan(uint32_t x, uint32_t* s_warp
   return x;
 }
 
-template <typename T>
+// 8 consecutive elements of a row, from one or two 16-byte loads when VEC (the row
+// start is 16-byte aligned) and the chunk lies inside the row, else element by element
+template <typename T, bool VEC>
+__device__ __forceinline__ void load8(const T* __restrict__ p, int v0, int V, T (&x)[8]) {
+  if (VEC && v0 + 8 <= V) {
+    constexpr int E = 16 / sizeof(T);
+#pragma unroll
+    for (int q = 0; q < 8 / E; ++q) {
+      const uint4 u = __ldg(reinterpret_cast<const uint4*>(p + v0) + q);
+      const T* e = reinterpret_cast<const T*>(&u);
+#pragma unroll
+      for (int i = 0; i < E; ++i) x[q * E + i] = e[i];
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) x[i] = v0 + i < V ? p[v0 + i] : T(0);
+  }
+}
+
+constexpr int TS_CAP = 2048;      // candidates one row may collect on the fast path
+constexpr int TS_SAMPLE = 8192;   // leading elements of a row that estimate a threshold
+
+// prefix|bin of the remaining-th largest key, given this pass's 256-bin histogram
+// (called by all 32 lanes of one warp; lane l owns bins [8l, 8l+8); writes
+// s_sel = {prefix, remaining, count above})
+__device__ __forceinline__ void radix_pick(const uint32_t* hist, uint32_t prefix, int shift,
+                                           uint32_t remaining, uint32_t above, uint32_t* s_sel) {
+  const int l = threadIdx.x % 32;
+  uint32_t h[8], mine = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) { h[i] = hist[8 * l + i]; mine += h[i]; }
+  // suffix sums over lanes: sum of bins >= 8l
+  uint32_t suf = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_down_sync(0xFFFFFFFFu, suf, o);
+    if (l + o < 32) suf += y;
+  }
+  // the bin lies in the highest lane whose suffix reaches `remaining` (lane 0 if none)
+  const uint32_t reach = __ballot_sync(0xFFFFFFFFu, suf >= remaining);
+  const int L = reach ? 31 - __clz(reach) : 0;
+  if (l == L) {
+    uint32_t cum = suf - mine;             // bins above this lane's range
+    int d = 8 * l + 7;
+    for (; d > 0; --d) {
+      const uint32_t hd = h[d - 8 * l];
+      if (cum + hd >= remaining || d == 8 * l) break;
+      cum += hd;
+    }
+    // d == 8l with the target not reached only happens in lane 0 (bin 0 takes the rest)
+    s_sel[0] = prefix | ((uint32_t)d << shift);
+    s_sel[1] = remaining - cum;
+    s_sel[2] = above + cum;
+  }
+}
+
+// Per draft row (one CTA of 512 threads):
+//  fast path (C <= TS_CAP / 2 and the id bitmaps fit in shared memory):
+//   1. t0 = the Ts-th largest key of the row's first TS_SAMPLE elements, Ts about
+//      twice the share of C the sample should hold, so that about 2C elements of the
+//      row have keys >= t0;
+//   2. one pass over the row collects (key, id) of every element with key >= t0 and
+//      the row's argmax;
+//   3. if C <= collected <= TS_CAP, the C-th largest key thr of the row is the C-th
+//      largest collected key (every key >= thr is >= t0), found by radix select over
+//      the collected keys; the candidates are all keys > thr plus the `quota` lowest
+//      ids with key == thr, marked in two id bitmaps and emitted in id order by a
+//      prefix count over the bitmaps;
+//  otherwise (and as fallback): radix select over the whole row, then an ordered
+//  compaction pass.
+template <typename T, bool VEC>
 __global__ void __launch_bounds__(TS_THREADS) topc_select_kernel(
-    const T* __restrict__ base, int64_t sn, int64_t sb, int Bm1, int B, int V, int C,
+    const T* __restrict__ base, int64_t sn, int64_t sb, int Bm1, int B, int V, int C, int fast_ok,
     int64_t* __restrict__ cand, T* __restrict__ base_c, int64_t* __restrict__ blk,
     const int64_t* __restrict__ anchor, uint32_t* err) {
   constexpr int KB = KeyBits<T>::value;
-  __shared__ uint32_t hist[256];
+  constexpr int NW = TS_THREADS / 32;
+  extern __shared__ __align__(16) uint32_t ts_dyn[];
+  uint32_t (*whist)[256] = reinterpret_cast<uint32_t (*)[256]>(ts_dyn);   // one histogram per warp
+  uint32_t* ckey = ts_dyn + NW * 256;
+  int* cid = reinterpret_cast<int*>(ckey + TS_CAP);
+  const int W = (V + 31) / 32;
+  uint32_t* gtm = reinterpret_cast<uint32_t*>(cid + TS_CAP);   // keys > thr, by id
+  uint32_t* eqm = gtm + W;                                      // keys == thr, by id
   __shared__ uint32_t s_warp[32];
   __shared__ uint32_t s_sel[3];   // prefix, remaining quota, count above the prefix
-  __shared__ float s_bv[TS_THREADS / 32];
-  __shared__ int s_bi[TS_THREADS / 32];
+  __shared__ uint32_t s_count;
+  __shared__ float s_bv[NW];
+  __shared__ int s_bi[NW];
   const int row = blockIdx.x;
   const int n = row / Bm1, b = row % Bm1;
   const T* p = base + (int64_t)n * sn + (int64_t)b * sb;
-  const int tid = threadIdx.x;
-
-  // ---- radix select of the C-th largest key, 8 bits at a time ----
-  uint32_t prefix = 0, pmask = 0, remaining = (uint32_t)C, above = 0;
-  for (int shift = KB - 8; shift >= 0; shift -= 8) {
-    for (int i = tid; i < 256; i += TS_THREADS) hist[i] = 0;
-    __syncthreads();
-    for (int v = tid; v < V; v += TS_THREADS) {
-      const uint32_t k = radix_key(p[v]);
-      if ((k & pmask) == prefix) atomicAdd(&hist[(k >> shift) & 255u], 1u);
-    }
-    __syncthreads();
-    if (tid == 0) {
-      uint32_t cum = 0;
-      int d = 255;
-      for (; d > 0; --d) {
-        if (cum + hist[d] >= remaining) break;
-        cum += hist[d];
-      }
-      s_sel[0] = prefix | ((uint32_t)d << shift);
-      s_sel[1] = remaining - cum;
-      s_sel[2] = above + cum;
-    }
-    __syncthreads();
-    prefix = s_sel[0];
-    remaining = s_sel[1];
-    above = s_sel[2];
-    pmask |= 255u << shift;
-    __syncthreads();
-  }
-  // keys > prefix: all `above` of them selected; keys == prefix: the first
-  // `remaining` in id order.
-  const uint32_t thr = prefix, quota = remaining;
-
-  // ---- ordered compaction in id order + the row argmax ----
-  uint32_t g_run = 0, e_run = 0;          // gt / eq counts of earlier chunks
-  float best = -INFINITY;
-  int bi = 0x7FFFFFFF;
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   int64_t* crow = cand + (int64_t)row * C;
   T* brow = base_c + (int64_t)row * C;
-  for (int c0 = 0; c0 < V; c0 += TS_THREADS * TS_ITEMS) {
-    const int v0 = c0 + tid * TS_ITEMS;
-    uint32_t keys[TS_ITEMS];
-    T vals[TS_ITEMS];
-    uint32_t ngt = 0, neq = 0;
+  float best = -INFINITY;
+  int bi = 0x7FFFFFFF;
+
+  // one radix step over keys supplied by `each(f)` (f(key) for every live key)
+  auto radix = [&](auto&& each, uint32_t need, uint32_t& thr_out, uint32_t& quota_out) {
+    uint32_t prefix = 0, pmask = 0, remaining = need, above = 0;
+    for (int shift = KB - 8; shift >= 0; shift -= 8) {
+      for (int i = tid; i < NW * 256; i += TS_THREADS) (&whist[0][0])[i] = 0;
+      __syncthreads();
+      each([&](uint32_t k) {
+        if ((k & pmask) == prefix) atomicAdd(&whist[warp][(k >> shift) & 255u], 1u);
+      });
+      __syncthreads();
+      if (tid < 256) {
+        uint32_t t = 0;
 #pragma unroll
-    for (int i = 0; i < TS_ITEMS; ++i) {
-      const int v = v0 + i;
-      if (v < V) {
-        vals[i] = p[v];
-        keys[i] = radix_key(vals[i]);
-        ngt += keys[i] > thr;
-        neq += keys[i] == thr;
-        const float x = to_f(vals[i]);
-        if (x > best) { best = x; bi = v; }
-      } else {
-        keys[i] = 0;
+        for (int w = 0; w < NW; ++w) t += whist[w][tid];
+        whist[0][tid] = t;
+      }
+      __syncthreads();
+      if (warp == 0) radix_pick(whist[0], prefix, shift, remaining, above, s_sel);
+      __syncthreads();
+      prefix = s_sel[0];
+      remaining = s_sel[1];
+      above = s_sel[2];
+      pmask |= 255u << shift;
+      __syncthreads();
+    }
+    thr_out = prefix;
+    quota_out = remaining;
+  };
+
+  bool fast = fast_ok != 0;
+  uint32_t thr = 0, quota = 0;
+  if (fast) {
+    // ---- 1. threshold estimate from the leading sample ----
+    const int Sn = min(TS_SAMPLE, V);
+    const uint32_t Ts =
+        (uint32_t)min((int64_t)Sn, (2 * (int64_t)C * Sn + V - 1) / V + 16);
+    uint32_t sk[TS_SAMPLE / TS_THREADS];
+#pragma unroll
+    for (int h = 0; h < TS_SAMPLE / TS_THREADS / 8; ++h) {
+      T x[8];
+      const int v0 = tid * (TS_SAMPLE / TS_THREADS) + h * 8;
+      load8<T, VEC>(p, v0, Sn, x);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) sk[h * 8 + i] = v0 + i < Sn ? radix_key(x[i]) : 0xFFFFFFFFu;
+    }
+    uint32_t t0, unused;
+    radix([&](auto&& f) {
+#pragma unroll
+      for (int i = 0; i < TS_SAMPLE / TS_THREADS; ++i)
+        if (sk[i] != 0xFFFFFFFFu) f(sk[i]);
+    }, Ts, t0, unused);
+
+    // ---- 2. collect every element with key >= t0: a chunk of 8 is looked at one by
+    // one only when its maximum reaches the threshold (about 2C of V elements do) ----
+    if (tid == 0) s_count = 0;
+    __syncthreads();
+    const float t0v = key_value(t0, (T*)nullptr);
+    for (int v0 = tid * 8; v0 < V; v0 += TS_THREADS * 8) {
+      T x[8];
+      load8<T, VEC>(p, v0, V, x);            // past-the-row slots read as 0: checked below
+      if (max8(x) >= t0v) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int v = v0 + i;
+          if (v < V && to_f(x[i]) >= t0v) {
+            const uint32_t slot = atomicAdd(&s_count, 1u);
+            if (slot < (uint32_t)TS_CAP) { ckey[slot] = radix_key(x[i]); cid[slot] = v; }
+          }
+        }
       }
     }
-    uint32_t tot;
-    const uint32_t incl = block_incl_scan(ngt | (neq << 16), s_warp, &tot);
-    const uint32_t excl = incl - (ngt | (neq << 16));
-    uint32_t gb = g_run + (excl & 0xFFFFu), eb = e_run + (excl >> 16);
-    uint32_t pos = gb + min(eb, quota);
-#pragma unroll
-    for (int i = 0; i < TS_ITEMS; ++i) {
-      const int v = v0 + i;
-      if (v >= V) break;
-      bool take = false;
-      if (keys[i] > thr) take = true;
-      else if (keys[i] == thr) { take = eb < quota; ++eb; }
-      if (take) { crow[pos] = v; brow[pos] = vals[i]; ++pos; }
+    __syncthreads();
+    const uint32_t ncol = s_count;
+    fast = ncol >= (uint32_t)C && ncol <= (uint32_t)TS_CAP;   // CTA-uniform
+
+    if (fast) {
+      // the row maximum is among the collected keys (it is >= t0): its lowest id
+      for (uint32_t j = tid; j < ncol; j += TS_THREADS) {
+        const float xv = key_value(ckey[j], (T*)nullptr);
+        if (better(xv, cid[j], best, bi)) { best = xv; bi = cid[j]; }
+      }
+      // ---- 3. the C-th largest collected key, then the id bitmaps ----
+      radix([&](auto&& f) {
+        for (uint32_t j = tid; j < ncol; j += TS_THREADS) f(ckey[j]);
+      }, (uint32_t)C, thr, quota);
+      for (int w = tid; w < 2 * W; w += TS_THREADS) gtm[w] = 0;
+      __syncthreads();
+      for (uint32_t j = tid; j < ncol; j += TS_THREADS) {
+        const uint32_t k = ckey[j];
+        const int id = cid[j];
+        if (k > thr) atomicOr(&gtm[id >> 5], 1u << (id & 31));
+        else if (k == thr) atomicOr(&eqm[id >> 5], 1u << (id & 31));
+      }
+      __syncthreads();
+      // keep the `quota` lowest ids of the boundary key, add them to the selection
+      const int wpt = (W + TS_THREADS - 1) / TS_THREADS, w0 = tid * wpt, w1 = min(W, w0 + wpt);
+      uint32_t cnt = 0;
+      for (int w = w0; w < w1; ++w) cnt += __popc(eqm[w]);
+      uint32_t tot;
+      uint32_t rank = block_incl_scan(cnt, s_warp, &tot) - cnt;
+      for (int w = w0; w < w1; ++w) {
+        uint32_t m = eqm[w], keep = 0;
+        while (m) {
+          const uint32_t bit = m & (0u - m);
+          if (rank < quota) keep |= bit;
+          ++rank;
+          m ^= bit;
+        }
+        gtm[w] |= keep;
+      }
+      __syncthreads();
+      // emit the selection in id order
+      cnt = 0;
+      for (int w = w0; w < w1; ++w) cnt += __popc(gtm[w]);
+      uint32_t pos = block_incl_scan(cnt, s_warp, &tot) - cnt;
+      for (int w = w0; w < w1; ++w) {
+        uint32_t m = gtm[w];
+        while (m) {
+          const int id = w * 32 + (__ffs(m) - 1);
+          crow[pos] = id;
+          brow[pos] = p[id];
+          ++pos;
+          m &= m - 1;
+        }
+      }
     }
-    g_run += tot & 0xFFFFu;
-    e_run += tot >> 16;
+  }
+
+  if (!fast) {
+    // ---- fallback: radix select over the whole row ----
+    radix([&](auto&& f) {
+      for (int c0 = 0; c0 < V; c0 += TS_THREADS * 8) {
+        const int v0 = c0 + tid * 8;
+        T x[8];
+        load8<T, VEC>(p, v0, V, x);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          if (v0 + i < V) f(radix_key(x[i]));
+      }
+    }, (uint32_t)C, thr, quota);
+    // keys > thr: all selected; keys == thr: the first `quota` in id order
+
+    // ---- ordered compaction in id order + the row argmax ----
+    uint32_t g_run = 0, e_run = 0;          // gt / eq counts of earlier chunks
+    best = -INFINITY;
+    bi = 0x7FFFFFFF;
+    for (int c0 = 0; c0 < V; c0 += TS_THREADS * TS_ITEMS) {
+      const int v0 = c0 + tid * TS_ITEMS;
+      uint32_t keys[TS_ITEMS];
+      T vals[TS_ITEMS];
+      uint32_t ngt = 0, neq = 0;
+      load8<T, VEC>(p, v0, V, vals);
+#pragma unroll
+      for (int i = 0; i < TS_ITEMS; ++i) {
+        const int v = v0 + i;
+        if (v < V) {
+          keys[i] = radix_key(vals[i]);
+          ngt += keys[i] > thr;
+          neq += keys[i] == thr;
+          const float x = to_f(vals[i]);
+          if (x > best) { best = x; bi = v; }
+        } else {
+          keys[i] = 0;
+        }
+      }
+      uint32_t tot;
+      const uint32_t incl = block_incl_scan(ngt | (neq << 16), s_warp, &tot);
+      const uint32_t excl = incl - (ngt | (neq << 16));
+      uint32_t gb = g_run + (excl & 0xFFFFu), eb = e_run + (excl >> 16);
+      uint32_t pos = gb + min(eb, quota);
+#pragma unroll
+      for (int i = 0; i < TS_ITEMS; ++i) {
+        const int v = v0 + i;
+        if (v >= V) break;
+        bool take = false;
+        if (keys[i] > thr) take = true;
+        else if (keys[i] == thr) { take = eb < quota; ++eb; }
+        if (take) { crow[pos] = v; brow[pos] = vals[i]; ++pos; }
+      }
+      g_run += tot & 0xFFFFu;
+      e_run += tot >> 16;
+    }
   }
   if (blk) {
     warp_argmax(best, bi);
-    if (tid % 32 == 0) { s_bv[tid / 32] = best; s_bi[tid / 32] = bi; }
+    if (lane == 0) { s_bv[warp] = best; s_bi[warp] = bi; }
     __syncthreads();
     if (tid < 32) {
-      best = tid < TS_THREADS / 32 ? s_bv[tid] : -INFINITY;
-      bi = tid < TS_THREADS / 32 ? s_bi[tid] : 0x7FFFFFFF;
+      best = tid < NW ? s_bv[tid] : -INFINITY;
+      bi = tid < NW ? s_bi[tid] : 0x7FFFFFFF;
       warp_argmax(best, bi);
       if (tid == 0) {
         blk[(int64_t)n * B + 1 + b] = bi;
@@ -253,21 +465,37 @@ cudaError_t xp_launch_topc_gather(const xp_head* h, const void* base, int64_t sn
                                   int C, int64_t* cand, void* base_c, void* w2c, int64_t* blk,
                                   const int64_t* anchor, cudaStream_t s) {
   const int Bm1 = h->B - 1, rows = N * Bm1;
-  if (h->dtype == XP_BF16)
-    topc_select_kernel<bf16><<<rows, TS_THREADS, 0, s>>>((const bf16*)base, sn, sb, Bm1, h->B,
-                                                         h->V, C, cand, (bf16*)base_c, blk, anchor,
-                                                         h->err);
-  else
-    topc_select_kernel<float><<<rows, TS_THREADS, 0, s>>>((const float*)base, sn, sb, Bm1, h->B,
-                                                          h->V, C, cand, (float*)base_c, blk,
-                                                          anchor, h->err);
-  cudaError_t e = cudaGetLastError();
+  const int E = (int)(16 / xp_elem(h->dtype));
+  // 16-byte loads need every row start 16-byte aligned
+  const bool vec = (uintptr_t)base % 16 == 0 && sn % E == 0 && sb % E == 0;
+  // fast path: room for the collected candidates and two id bitmaps in shared memory
+  const size_t smem_hist = (size_t)(TS_THREADS / 32) * 256 * 4;
+  const size_t smem_fast = smem_hist + (size_t)TS_CAP * 8 + (size_t)2 * ((h->V + 31) / 32) * 4;
+  const bool fast = C <= TS_CAP / 2 && smem_fast <= 160 * 1024;
+  const size_t smem = fast ? smem_fast : smem_hist;
+  cudaError_t e = cudaSuccess;
+#define XP_SELECT(T, VEC)                                                                   \
+  do {                                                                                      \
+    e = cudaFuncSetAttribute(topc_select_kernel<T, VEC>,                                    \
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);       \
+    if (e != cudaSuccess) return e;                                                         \
+    topc_select_kernel<T, VEC><<<rows, TS_THREADS, smem, s>>>(                              \
+        (const T*)base, sn, sb, Bm1, h->B, h->V, C, fast ? 1 : 0, cand, (T*)base_c, blk,    \
+        anchor, h->err);                                                                    \
+  } while (0)
+  if (h->dtype == XP_BF16) {
+    if (vec) XP_SELECT(bf16, true); else XP_SELECT(bf16, false);
+  } else {
+    if (vec) XP_SELECT(float, true); else XP_SELECT(float, false);
+  }
+#undef XP_SELECT
+  e = cudaGetLastError();
   if (e != cudaSuccess || !w2c) return e;
   const int row_bytes = (int)(h->r * xp_elem(h->dtype));
   const int64_t total = (int64_t)rows * C;
   const int grid = (int)std::min<int64_t>((total + 7) / 8, (int64_t)h->num_sms * 16);
-  const bool vec = row_bytes % 16 == 0 && (uintptr_t)w2c % 16 == 0;
-  if (vec)
+  const bool vec_rows = row_bytes % 16 == 0 && (uintptr_t)w2c % 16 == 0;
+  if (vec_rows)
     gather_rows_kernel<true><<<grid, 256, 0, s>>>((const char*)h->w2, cand, (char*)w2c, total,
                                                   row_bytes, h->V, h->err);
   else
