@@ -30,6 +30,24 @@ __device__ __forceinline__ float key_value(uint32_t k, bf16*) {
 __device__ __forceinline__ float key_value(uint32_t k, float*) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
+// bit i set when x[i] >= t (packed bf16 pair compares for bf16)
+__device__ __forceinline__ uint32_t ge_mask8(const bf16 (&x)[8], float t) {
+  const __nv_bfloat162* v = reinterpret_cast<const __nv_bfloat162*>(x);
+  const __nv_bfloat162 t2 = __float2bfloat162_rn(t);   // t is a bf16 value: exact
+  uint32_t m = 0;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint32_t g = __hge2_mask(v[q], t2);            // 0xFFFF per true half
+    m |= ((g & 1u) | ((g >> 15) & 2u)) << (2 * q);
+  }
+  return m;
+}
+__device__ __forceinline__ uint32_t ge_mask8(const float (&x)[8], float t) {
+  uint32_t m = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) m |= (x[i] >= t ? 1u : 0u) << i;
+  return m;
+}
 // largest of 8 values (packed bf16 pairs for bf16)
 __device__ __forceinline__ float max8(const bf16 (&x)[8]) {
   const __nv_bfloat162* v = reinterpret_cast<const __nv_bfloat162*>(x);
@@ -93,6 +111,7 @@ __device__ __forceinline__ void load8(const T* __restrict__ p, int v0, int V, T 
 }
 
 constexpr int TS_CAP = 2048;      // candidates one row may collect on the fast path
+constexpr int TS_HISTS = 4;       // radix histograms per CTA (shared by TS_THREADS/32/TS_HISTS warps)
 constexpr int TS_SAMPLE = 8192;   // leading elements of a row that estimate a threshold
 
 // prefix|bin of the remaining-th largest key, given this pass's 256-bin histogram
@@ -139,24 +158,25 @@ __device__ __forceinline__ void radix_pick(const uint32_t* hist, uint32_t prefix
 //   3. if C <= collected <= TS_CAP, the C-th largest key thr of the row is the C-th
 //      largest collected key (every key >= thr is >= t0), found by radix select over
 //      the collected keys; the candidates are all keys > thr plus the `quota` lowest
-//      ids with key == thr, marked in two id bitmaps and emitted in id order by a
-//      prefix count over the bitmaps;
+//      ids with key == thr (ranked among themselves), marked in an id bitmap and
+//      emitted in id order by a prefix count over the bitmap;
 //  otherwise (and as fallback): radix select over the whole row, then an ordered
 //  compaction pass.
 template <typename T, bool VEC>
-__global__ void __launch_bounds__(TS_THREADS) topc_select_kernel(
+__global__ void __launch_bounds__(TS_THREADS, 2) topc_select_kernel(
     const T* __restrict__ base, int64_t sn, int64_t sb, int Bm1, int B, int V, int C, int fast_ok,
     int64_t* __restrict__ cand, T* __restrict__ base_c, int64_t* __restrict__ blk,
     const int64_t* __restrict__ anchor, uint32_t* err) {
   constexpr int KB = KeyBits<T>::value;
   constexpr int NW = TS_THREADS / 32;
   extern __shared__ __align__(16) uint32_t ts_dyn[];
-  uint32_t (*whist)[256] = reinterpret_cast<uint32_t (*)[256]>(ts_dyn);   // one histogram per warp
-  uint32_t* ckey = ts_dyn + NW * 256;
+  // TS_HISTS histograms, each shared by the warps w with w % TS_HISTS equal
+  uint32_t (*whist)[256] = reinterpret_cast<uint32_t (*)[256]>(ts_dyn);
+  uint32_t* ckey = ts_dyn + TS_HISTS * 256;
   int* cid = reinterpret_cast<int*>(ckey + TS_CAP);
+  int* eqid = cid + TS_CAP;                                     // ids whose key == thr
   const int W = (V + 31) / 32;
-  uint32_t* gtm = reinterpret_cast<uint32_t*>(cid + TS_CAP);   // keys > thr, by id
-  uint32_t* eqm = gtm + W;                                      // keys == thr, by id
+  uint32_t* selm = reinterpret_cast<uint32_t*>(eqid + TS_CAP);  // selected ids, one bit each
   __shared__ uint32_t s_warp[32];
   __shared__ uint32_t s_sel[3];   // prefix, remaining quota, count above the prefix
   __shared__ uint32_t s_count;
@@ -175,16 +195,16 @@ __global__ void __launch_bounds__(TS_THREADS) topc_select_kernel(
   auto radix = [&](auto&& each, uint32_t need, uint32_t& thr_out, uint32_t& quota_out) {
     uint32_t prefix = 0, pmask = 0, remaining = need, above = 0;
     for (int shift = KB - 8; shift >= 0; shift -= 8) {
-      for (int i = tid; i < NW * 256; i += TS_THREADS) (&whist[0][0])[i] = 0;
+      for (int i = tid; i < TS_HISTS * 256; i += TS_THREADS) (&whist[0][0])[i] = 0;
       __syncthreads();
       each([&](uint32_t k) {
-        if ((k & pmask) == prefix) atomicAdd(&whist[warp][(k >> shift) & 255u], 1u);
+        if ((k & pmask) == prefix) atomicAdd(&whist[warp % TS_HISTS][(k >> shift) & 255u], 1u);
       });
       __syncthreads();
       if (tid < 256) {
         uint32_t t = 0;
 #pragma unroll
-        for (int w = 0; w < NW; ++w) t += whist[w][tid];
+        for (int w = 0; w < TS_HISTS; ++w) t += whist[w][tid];
         whist[0][tid] = t;
       }
       __syncthreads();
@@ -228,16 +248,57 @@ __global__ void __launch_bounds__(TS_THREADS) topc_select_kernel(
     if (tid == 0) s_count = 0;
     __syncthreads();
     const float t0v = key_value(t0, (T*)nullptr);
-    for (int v0 = tid * 8; v0 < V; v0 += TS_THREADS * 8) {
-      T x[8];
-      load8<T, VEC>(p, v0, V, x);            // past-the-row slots read as 0: checked below
-      if (max8(x) >= t0v) {
+    auto keep = [&](uint32_t k, int v) {
+      const uint32_t slot = atomicAdd(&s_count, 1u);
+      if (slot < (uint32_t)TS_CAP) { ckey[slot] = k; cid[slot] = v; }
+    };
+    if constexpr (VEC && sizeof(T) == 2) {
+      // bf16 rows: 8 raw 16-byte words per thread in flight, packed-pair tests
+      constexpr int U = 8;
+      const __nv_bfloat162 t2 = __float2bfloat162_rn(t0v);   // t0v is a bf16 value: exact
+      for (int c0 = tid * 8; c0 < V; c0 += U * TS_THREADS * 8) {
+        uint4 w[U];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int v = v0 + i;
-          if (v < V && to_f(x[i]) >= t0v) {
-            const uint32_t slot = atomicAdd(&s_count, 1u);
-            if (slot < (uint32_t)TS_CAP) { ckey[slot] = radix_key(x[i]); cid[slot] = v; }
+        for (int u = 0; u < U; ++u) {
+          const int v0 = c0 + u * TS_THREADS * 8;
+          w[u] = v0 + 8 <= V ? __ldg(reinterpret_cast<const uint4*>(p + v0))
+                             : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int v0 = c0 + u * TS_THREADS * 8;
+          const uint32_t q[4] = {w[u].x, w[u].y, w[u].z, w[u].w};
+          const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(q);
+          const __nv_bfloat162 m2 = __hmax2(__hmax2(h2[0], h2[1]), __hmax2(h2[2], h2[3]));
+          if (fmaxf(__low2float(m2), __high2float(m2)) >= t0v && v0 + 8 <= V) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const uint32_t g = __hge2_mask(h2[e], t2);
+              if (g & 1u) keep(radix_key(__low2bfloat16(h2[e])), v0 + 2 * e);
+              if (g & 0x10000u) keep(radix_key(__high2bfloat16(h2[e])), v0 + 2 * e + 1);
+            }
+          }
+        }
+      }
+      // the ragged end of the row (fewer than 8 elements), element by element
+      for (int v = (V / 8) * 8 + tid; v < V; v += TS_THREADS)
+        if (to_f(p[v]) >= t0v) keep(radix_key(p[v]), v);
+    } else {
+      constexpr int U = 4;                     // chunks of 8 in flight
+      for (int c0 = tid * 8; c0 < V; c0 += U * TS_THREADS * 8) {
+        T x[U][8];
+#pragma unroll
+        for (int u = 0; u < U; ++u)            // past-the-row slots read as 0: checked below
+          load8<T, VEC>(p, c0 + u * TS_THREADS * 8, V, x[u]);
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int v0 = c0 + u * TS_THREADS * 8;
+          if (max8(x[u]) >= t0v) {
+            uint32_t m = ge_mask8(x[u], t0v);
+            if (v0 + 8 > V) m &= (1u << max(0, V - v0)) - 1u;   // slots past the row
+#pragma unroll
+            for (int i = 0; i < 8; ++i)                          // static indices: registers
+              if (m & (1u << i)) keep(radix_key(x[u][i]), v0 + i);
           }
         }
       }
@@ -256,38 +317,33 @@ __global__ void __launch_bounds__(TS_THREADS) topc_select_kernel(
       radix([&](auto&& f) {
         for (uint32_t j = tid; j < ncol; j += TS_THREADS) f(ckey[j]);
       }, (uint32_t)C, thr, quota);
-      for (int w = tid; w < 2 * W; w += TS_THREADS) gtm[w] = 0;
+      if (tid == 0) s_count = 0;
+      for (int w = tid; w < W; w += TS_THREADS) selm[w] = 0;
       __syncthreads();
       for (uint32_t j = tid; j < ncol; j += TS_THREADS) {
         const uint32_t k = ckey[j];
         const int id = cid[j];
-        if (k > thr) atomicOr(&gtm[id >> 5], 1u << (id & 31));
-        else if (k == thr) atomicOr(&eqm[id >> 5], 1u << (id & 31));
+        if (k > thr) atomicOr(&selm[id >> 5], 1u << (id & 31));
+        else if (k == thr) eqid[atomicAdd(&s_count, 1u)] = id;
       }
       __syncthreads();
-      // keep the `quota` lowest ids of the boundary key, add them to the selection
+      // of the boundary key, the `quota` lowest ids: rank each by the lower ids
+      const uint32_t neq = s_count;
+      for (uint32_t j = tid; j < neq; j += TS_THREADS) {
+        const int id = eqid[j];
+        uint32_t rank = 0;
+        for (uint32_t i = 0; i < neq; ++i) rank += eqid[i] < id;
+        if (rank < quota) atomicOr(&selm[id >> 5], 1u << (id & 31));
+      }
+      __syncthreads();
       const int wpt = (W + TS_THREADS - 1) / TS_THREADS, w0 = tid * wpt, w1 = min(W, w0 + wpt);
-      uint32_t cnt = 0;
-      for (int w = w0; w < w1; ++w) cnt += __popc(eqm[w]);
-      uint32_t tot;
-      uint32_t rank = block_incl_scan(cnt, s_warp, &tot) - cnt;
-      for (int w = w0; w < w1; ++w) {
-        uint32_t m = eqm[w], keep = 0;
-        while (m) {
-          const uint32_t bit = m & (0u - m);
-          if (rank < quota) keep |= bit;
-          ++rank;
-          m ^= bit;
-        }
-        gtm[w] |= keep;
-      }
-      __syncthreads();
+      uint32_t cnt, tot;
       // emit the selection in id order
       cnt = 0;
-      for (int w = w0; w < w1; ++w) cnt += __popc(gtm[w]);
+      for (int w = w0; w < w1; ++w) cnt += __popc(selm[w]);
       uint32_t pos = block_incl_scan(cnt, s_warp, &tot) - cnt;
       for (int w = w0; w < w1; ++w) {
-        uint32_t m = gtm[w];
+        uint32_t m = selm[w];
         while (m) {
           const int id = w * 32 + (__ffs(m) - 1);
           crow[pos] = id;
@@ -379,6 +435,27 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const char* __restrict
   const int lane = threadIdx.x % 32;
   const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / 32;
   const int64_t nwarps = (int64_t)gridDim.x * blockDim.x / 32;
+  if (VEC && row_bytes == 32 * 16) {
+    // one 16-byte piece per lane and row; 4 rows per step so that 4 loads are in flight
+    constexpr int U = 4;
+    for (int64_t k0 = warp0; k0 < total; k0 += U * nwarps) {
+      int64_t id[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int64_t k = k0 + u * nwarps;
+        id[u] = k < total ? checked_token(cand[k], V, err) : -1;
+      }
+      uint4 v[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        if (id[u] >= 0) v[u] = __ldg(reinterpret_cast<const uint4*>(w2 + id[u] * row_bytes) + lane);
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        if (id[u] >= 0)
+          reinterpret_cast<uint4*>(w2c + (k0 + u * nwarps) * row_bytes)[lane] = v[u];
+    }
+    return;
+  }
   for (int64_t k = warp0; k < total; k += nwarps) {
     const int64_t id = checked_token(cand[k], V, err);
     const char* src = w2 + id * row_bytes;
@@ -468,9 +545,9 @@ cudaError_t xp_launch_topc_gather(const xp_head* h, const void* base, int64_t sn
   const int E = (int)(16 / xp_elem(h->dtype));
   // 16-byte loads need every row start 16-byte aligned
   const bool vec = (uintptr_t)base % 16 == 0 && sn % E == 0 && sb % E == 0;
-  // fast path: room for the collected candidates and two id bitmaps in shared memory
-  const size_t smem_hist = (size_t)(TS_THREADS / 32) * 256 * 4;
-  const size_t smem_fast = smem_hist + (size_t)TS_CAP * 8 + (size_t)2 * ((h->V + 31) / 32) * 4;
+  // fast path: room for the collected candidates, the boundary ids and an id bitmap
+  const size_t smem_hist = (size_t)TS_HISTS * 256 * 4;
+  const size_t smem_fast = smem_hist + (size_t)TS_CAP * 12 + (size_t)((h->V + 31) / 32) * 4;
   const bool fast = C <= TS_CAP / 2 && smem_fast <= 160 * 1024;
   const size_t smem = fast ? smem_fast : smem_hist;
   cudaError_t e = cudaSuccess;
