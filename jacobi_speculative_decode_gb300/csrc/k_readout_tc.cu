@@ -2,20 +2,28 @@
 // (xpress kernels page, fused_add_argmax_to_blk with the w2 matmul of refine_bias fused in).
 //
 // One CTA owns a tile of up to 128 draft rows (whole blocks only) and a
-// contiguous range of 256-wide vocabulary tiles.  Per vocabulary tile:
-//   TMA   w2[v-tile, k-chunk]  (256 x 64 bf16, 128B-swizzled)  -> 3-stage smem ring
-//   TMA   base[rows, 64 ids]   (one box per quarter tile)        -> 4-stage smem ring
-//   MMA   tcgen05 M=128 (rows) x N=256 (vocab) x K=r, fp32 accumulators in TMEM,
-//         double-buffered (2 x 256 columns)
+// contiguous range of 192-wide vocabulary tiles.  The latent tile (128 rows x r)
+// lives in tensor memory as the MMA's A operand, so shared memory holds only the
+// two streams.  Per vocabulary tile:
+//   TMA   w2[v-tile, k-chunk]  (192 x 64 bf16, 128B-swizzled)  -> 5-stage smem ring
+//   TMA   base[rows, 64 ids]   (one box per 64-id third)        -> 6-stage smem ring
+//         (two tiles: the next tile's base is in flight while this one is reduced)
+//   MMA   tcgen05 M=128 (rows) x N=192 (vocab) x K=r, A from TMEM, fp32 accumulators
+//         in TMEM, double-buffered (2 x 192 columns; A takes the last 128 columns)
 //   epilogue: each thread owns one row (one TMEM lane), adds base, keeps a
 //         running (max, lowest id) -- the logits never leave the SM.
-// The latent tile stays resident in smem for the whole kernel.  Per-row winners
-// of all CTAs of a row tile merge through a packed atomicMax; the CTA that
-// arrives last publishes into blk and resets the partials.
+// Per-row winners of all CTAs of a row tile merge through a packed atomicMax;
+// the CTA that arrives last publishes into blk and resets the partials.
 //
-// Warp roles (352 threads): warp 0 base producer, warp 1 MMA issuer (+ TMEM
-// owner), warp 2 w2 producer, warps 3..10 epilogue: warp w reads TMEM lane
-// group w % 4 and half (w - 3) / 4 of every tile.
+// Warp roles (480 threads): warp 0 base producer, warp 1 MMA issuer (+ TMEM
+// owner), warp 2 w2 producer, warps 3..14 epilogue: warp w reads TMEM lane
+// group w % 4 and third (w - 3) / 4 of every tile; the epilogue warps also write
+// the latent tile into TMEM before the first MMA.
+//
+// Every base stage is consumed by one fixed group of four warps (the ring size is a
+// multiple of the thirds per tile), and a group consumes its stages in order, so no
+// consumer ever waits on a stage more than one phase ahead of the phase it is in:
+// an mbarrier parity wait cannot tell a later phase from the previous one.
 #include <algorithm>
 
 #include "sm100_ptx.cuh"
@@ -26,17 +34,21 @@ using namespace xpd;
 namespace {
 
 constexpr int BM = 128;           // rows per MMA (TMEM lanes)
-constexpr int BN = 256;           // vocabulary ids per tile (MMA N)
+constexpr int BN = 192;           // vocabulary ids per tile (MMA N)
 constexpr int BK = 64;            // k per swizzled chunk (128 bytes of bf16)
-constexpr int W2_STAGES = 3;      // k-chunks of w2 in flight (w2 is 2/3 of each SM's stream)
-constexpr int BASE_STAGES = 4;    // 64-id quarters of base in flight (one tile)
-constexpr int QPT = BN / 64;      // base quarters per tile
-constexpr int A_CHUNK_BYTES = BM * BK * 2;          // 16 KB
-constexpr int W2_STAGE_BYTES = BN * BK * 2;         // 32 KB
+constexpr int QPT = BN / 64;      // 64-id thirds per tile
+constexpr int W2_STAGES = 5;      // k-chunks of w2 in flight
+constexpr int BASE_STAGES = 2 * QPT;  // two tiles of base in flight; stage s always holds
+                                      // third s % QPT, so each has a single consumer group
+constexpr int EPI_WARPS = 4 * QPT;                  // one warp per (lane quadrant, third)
+constexpr int W2_STAGE_BYTES = BN * BK * 2;         // 24 KB
 constexpr int BASE_STAGE_BYTES = 128 * 64 * 2;      // 16 KB: one 64-wide box of <= 128 rows
-constexpr int NUM_THREADS = 352;   // 3 producer/MMA warps + 8 epilogue warps
-constexpr uint32_t TMEM_COLS = 2 * BN;   // double-buffered accumulator
+constexpr int NUM_THREADS = (3 + EPI_WARPS) * 32;   // 480
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t A_COL = 2 * BN;                  // latent tile: columns [384, 384 + r/2)
 constexpr uint32_t IDESC = ptx::idesc_bf16_f32(BM, BN);
+static_assert(A_COL + 128 <= TMEM_COLS, "accumulators and the latent tile share TMEM");
+static_assert(BASE_STAGES % QPT == 0, "a base stage always holds the same third");
 
 struct Bars {
   uint64_t a_full;
@@ -59,7 +71,7 @@ __device__ __forceinline__ float bf16hi(uint32_t u) { return __uint_as_float(u &
 // commits arrive on the stage's empty barrier in every CTA of the cluster).
 template <int KCH, int MC>
 __global__ void __launch_bounds__(NUM_THREADS, 1) readout_tc_kernel(
-    const __grid_constant__ CUtensorMap tm_lat, const __grid_constant__ CUtensorMap tm_w2,
+    const __nv_bfloat16* __restrict__ lat, const __grid_constant__ CUtensorMap tm_w2,
     const __grid_constant__ CUtensorMap tm_base, int rows, int Bm1, int B, int V, int rpt, int bpt,
     int n_rt, int n_seg, int nvt, int64_t* __restrict__ blk, float* __restrict__ win,
     const float* __restrict__ pf_rows, int pf_row_bytes,
@@ -67,8 +79,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) readout_tc_kernel(
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = ptx::smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
-  uint8_t* sA = smem;                                    // KCH x 16 KB
-  uint8_t* sW = sA + KCH * A_CHUNK_BYTES;                // W2_STAGES x 32 KB
+  uint8_t* sW = smem;                                    // W2_STAGES x 24 KB
   uint8_t* sC = sW + W2_STAGES * W2_STAGE_BYTES;         // BASE_STAGES x 16 KB
   Bars* bars = reinterpret_cast<Bars*>(sC + BASE_STAGES * BASE_STAGE_BYTES);
   volatile int* abort = &bars->abort;
@@ -79,18 +90,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) readout_tc_kernel(
   const int row0 = tile * rpt;
 
   if (threadIdx.x == 0) {
-    ptx::mbar_init(ptx::smem_u32(&bars->a_full), 1);
+    ptx::mbar_init(ptx::smem_u32(&bars->a_full), EPI_WARPS);   // every epilogue warp
     for (int s = 0; s < W2_STAGES; ++s) {
       ptx::mbar_init(ptx::smem_u32(&bars->w_full[s]), 1);
       ptx::mbar_init(ptx::smem_u32(&bars->w_empty[s]), MC);   // one MMA commit per CTA
     }
     for (int s = 0; s < BASE_STAGES; ++s) {
       ptx::mbar_init(ptx::smem_u32(&bars->c_full[s]), 1);
-      ptx::mbar_init(ptx::smem_u32(&bars->c_empty[s]), 4);   // the 4 warps of one half
+      ptx::mbar_init(ptx::smem_u32(&bars->c_empty[s]), 4);   // the 4 warps of one third
     }
     for (int s = 0; s < 2; ++s) {
       ptx::mbar_init(ptx::smem_u32(&bars->t_full[s]), 1);
-      ptx::mbar_init(ptx::smem_u32(&bars->t_empty[s]), 8);   // all 8 epilogue warps
+      ptx::mbar_init(ptx::smem_u32(&bars->t_empty[s]), EPI_WARPS);
     }
     ptx::mbar_init(ptx::smem_u32(&bars->mma_done), 1);
     bars->abort = 0;
@@ -122,7 +133,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) readout_tc_kernel(
       int ci = 0;
       bool ok = true;
       for (int vt = vt0; vt < vt1 && ok; ++vt) {
-        for (int qt = 0; qt < BN / 64 && ok; ++qt, ++ci) {
+        for (int qt = 0; qt < QPT && ok; ++qt, ++ci) {
           const int s = ci % BASE_STAGES;
           ok = ptx::mbar_wait(ptx::smem_u32(&bars->c_empty[s]), ((ci / BASE_STAGES) & 1) ^ 1,
                               abort, err);
@@ -142,27 +153,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) readout_tc_kernel(
         }
     }
   } else if (warp == 2) {
-    // ---------------- latent + w2 producer ----------------
+    // ---------------- w2 producer (w2 depends on nothing earlier in the stream) ----------
     if (lane == 0) {
-      ptx::prefetch_tmap(&tm_lat);
       ptx::prefetch_tmap(&tm_w2);
       const uint64_t pol_keep = ptx::policy_evict_last();
-      const uint32_t a_full = ptx::smem_u32(&bars->a_full);
       uint32_t issued[W2_STAGES] = {};
       int wi = 0;
       bool ok = true;
-      bool have_a = false;
       for (int vt = vt0; vt < vt1 && ok; ++vt) {
         for (int kc = 0; kc < KCH; ++kc, ++wi) {
-          if (!have_a && wi == W2_STAGES) {
-            // w2 needs nothing from the previous kernel; the latents do
-            ptx::pdl_wait();
-            ptx::mbar_arrive_expect_tx(a_full, KCH * A_CHUNK_BYTES);
-            for (int k = 0; k < KCH; ++k)
-              ptx::tma_load_2d(ptx::smem_u32(sA + k * A_CHUNK_BYTES), &tm_lat, a_full, k * BK,
-                               row0, pol_keep);
-            have_a = true;
-          }
           const int s = wi % W2_STAGES;
           ok = ptx::mbar_wait(ptx::smem_u32(&bars->w_empty[s]), ((wi / W2_STAGES) & 1) ^ 1, abort,
                               err);
@@ -180,15 +179,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) readout_tc_kernel(
           ++issued[s];
         }
       }
-      if (!have_a) {
-        ptx::pdl_wait();
-        ptx::mbar_arrive_expect_tx(a_full, KCH * A_CHUNK_BYTES);
-        for (int k = 0; k < KCH; ++k)
-          ptx::tma_load_2d(ptx::smem_u32(sA + k * A_CHUNK_BYTES), &tm_lat, a_full, k * BK, row0,
-                           pol_keep);
-      }
       volatile int no_abort = 0;
-      ptx::mbar_wait(a_full, 0, &no_abort, err);
       for (int s = 0; s < W2_STAGES; ++s)
         if (issued[s])
           ptx::mbar_wait(ptx::smem_u32(&bars->w_full[s]), (issued[s] - 1) & 1, &no_abort, err);
@@ -210,12 +201,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) readout_tc_kernel(
           ok = ptx::mbar_wait(ptx::smem_u32(&bars->w_full[s]), (wi / W2_STAGES) & 1, abort, err);
           if (!ok) break;
           ptx::tc_fence_after();
-          const uint32_t a0 = ptx::smem_u32(sA + kc * A_CHUNK_BYTES);
           const uint32_t b0 = ptx::smem_u32(sW + s * W2_STAGE_BYTES);
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk)
-            ptx::mma_bf16(d, ptx::sw128_desc(a0 + kk * 32), ptx::sw128_desc(b0 + kk * 32), IDESC,
-                          (kc | kk) != 0);
+          for (int kk = 0; kk < BK / 16; ++kk)   // A: 16 k = 8 columns per step
+            ptx::mma_bf16_ts(d, tmem + A_COL + (uint32_t)(kc * 32 + kk * 8),
+                             ptx::sw128_desc(b0 + kk * 32), IDESC, (kc | kk) != 0);
           if (MC == 1)
             ptx::mma_commit(ptx::smem_u32(&bars->w_empty[s]));
           else
@@ -229,73 +219,106 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) readout_tc_kernel(
       ptx::mbar_wait(ptx::smem_u32(&bars->mma_done), 0, &no_abort, err);
     }
   } else {
-    // ---------------- epilogue: one row per thread, half of each tile per warp ----------------
-    static_assert(QPT % 2 == 0 && BASE_STAGES % QPT == 0, "quarters split evenly");
+    // ---------------- epilogue: one row per thread, a third of each tile per warp ----------
     const int g = warp & 3;                  // TMEM lane group this warp may access
-    const int half = (warp - 3) >> 2;        // which half of every tile's ids
+    const int third = (warp - 3) >> 2;       // which 64 ids of every tile
     const int i = g * 32 + lane;             // row within the tile
     const uint32_t trow = tmem + ((uint32_t)(g * 32) << 16);
+    {
+      // the latent tile into TMEM columns [A_COL, A_COL + r/2): k-chunk c (64 values =
+      // 32 columns) of the group's 32 rows is written by the warp with third == c % 3
+      ptx::pdl_wait();                       // lat comes from the previous kernel
+      const int grow = row0 + i;
+      const bool live = i < rpt && grow < rows;
+      const uint4* src = reinterpret_cast<const uint4*>(lat + (int64_t)(live ? grow : 0) * (KCH * BK));
+      uint4 q[2][8];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int c = third + QPT * j;
+        if (c < KCH)
+#pragma unroll
+          for (int e = 0; e < 8; ++e) q[j][e] = live ? __ldg(src + c * 8 + e) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int c = third + QPT * j;
+        if (c < KCH) {
+          uint32_t v[32];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            v[4 * e] = q[j][e].x;
+            v[4 * e + 1] = q[j][e].y;
+            v[4 * e + 2] = q[j][e].z;
+            v[4 * e + 3] = q[j][e].w;
+          }
+          ptx::tmem_st32(trow + A_COL + (uint32_t)(c * 32), v);
+        }
+      }
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->a_full));
+    }
     float best = -INFINITY;
     int bi = 0x7FFFFFFF;
     int ti = 0;
     bool ok = true;
     for (int vt = vt0; vt < vt1 && ok; ++vt, ++ti) {
+      const int ci = ti * QPT + third;       // this third's fill index in the base ring
+      const int st = ci % BASE_STAGES;
       const int buf = ti & 1;
       ok = ptx::mbar_wait(ptx::smem_u32(&bars->t_full[buf]), (ti >> 1) & 1, abort, err);
       ok = __all_sync(0xFFFFFFFFu, ok);      // warp-uniform: tcgen05.ld is .sync.aligned
       if (!ok) break;
       ptx::tc_fence_after();
       const int vbase = vt * BN;
-      for (int qq = 0; qq < QPT / 2 && ok; ++qq) {
-        const int qt = half * (QPT / 2) + qq;              // quarter within the tile
-        const int ci = ti * QPT + qt, st = ci % BASE_STAGES;  // its slot in the base ring
-        ok = ptx::mbar_wait(ptx::smem_u32(&bars->c_full[st]), (ci / BASE_STAGES) & 1, abort, err);
-        ok = __all_sync(0xFFFFFFFFu, ok);
-        if (!ok) break;
-        const uint8_t* rowp = sC + st * BASE_STAGE_BYTES + i * 128;
+      ok = ptx::mbar_wait(ptx::smem_u32(&bars->c_full[st]), (ci / BASE_STAGES) & 1, abort, err);
+      ok = __all_sync(0xFFFFFFFFu, ok);
+      if (!ok) break;
+      const uint8_t* rowp = sC + st * BASE_STAGE_BYTES + i * 128;
 #pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          const int col = qt * 64 + cc * 32;
-          uint32_t acc[32];
-          ptx::tmem_ld32(trow + (uint32_t)(buf * BN + col), acc);
-          ptx::tmem_wait_ld();
-          float sc[32];
+      for (int cc = 0; cc < 2; ++cc) {
+        const int col = third * 64 + cc * 32;
+        uint32_t acc[32];
+        ptx::tmem_ld32(trow + (uint32_t)(buf * BN + col), acc);
+        ptx::tmem_wait_ld();
+        float sc[32];
 #pragma unroll
-          for (int ch = 0; ch < 4; ++ch) {
-            const int lc = cc * 4 + ch;              // logical 16-byte chunk in the 128-byte row
-            const uint4 bv = *reinterpret_cast<const uint4*>(rowp + ((lc ^ (i & 7)) << 4));
-            const uint32_t w4[4] = {bv.x, bv.y, bv.z, bv.w};
+        for (int ch = 0; ch < 4; ++ch) {
+          const int lc = cc * 4 + ch;                // logical 16-byte chunk in the 128-byte row
+          const uint4 bv = *reinterpret_cast<const uint4*>(rowp + ((lc ^ (i & 7)) << 4));
+          const uint32_t w4[4] = {bv.x, bv.y, bv.z, bv.w};
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const float bval = (e & 1) ? bf16hi(w4[e >> 1]) : bf16lo(w4[e >> 1]);
-              sc[ch * 8 + e] = __uint_as_float(acc[ch * 8 + e]) + bval;
-            }
-          }
-          const int vlim = V - (vbase + col);        // ids at or past V are padding
-          if (vlim < 32) {                           // warp-uniform: only the last tile
-#pragma unroll
-            for (int e = 0; e < 32; ++e)
-              if (e >= vlim) sc[e] = -INFINITY;
-          }
-          // chunk maximum first; the lowest index of it only when it beats the row's best
-          float m = sc[0];
-#pragma unroll
-          for (int e = 1; e < 32; ++e) m = fmaxf(m, sc[e]);
-          if (m > best) {
-            int first = 31;
-#pragma unroll
-            for (int e = 31; e >= 0; --e)
-              if (sc[e] == m) first = e;
-            best = m;
-            bi = vbase + col + first;
+          for (int e = 0; e < 8; ++e) {
+            const float bval = (e & 1) ? bf16hi(w4[e >> 1]) : bf16lo(w4[e >> 1]);
+            sc[ch * 8 + e] = __uint_as_float(acc[ch * 8 + e]) + bval;
           }
         }
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->c_empty[st]));
+        const int vlim = V - (vbase + col);          // ids at or past V are padding
+        if (vlim < 32) {                             // warp-uniform: only the last tile
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (e >= vlim) sc[e] = -INFINITY;
+        }
+        // chunk maximum first; the lowest index of it only when it beats the row's best
+        float m = sc[0];
+#pragma unroll
+        for (int e = 1; e < 32; ++e) m = fmaxf(m, sc[e]);
+        if (m > best) {
+          int first = 31;
+#pragma unroll
+          for (int e = 31; e >= 0; --e)
+            if (sc[e] == m) first = e;
+          best = m;
+          bi = vbase + col + first;
+        }
       }
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0 && ok) ptx::mbar_arrive(ptx::smem_u32(&bars->t_empty[buf]));
+      if (lane == 0) {
+        ptx::mbar_arrive(ptx::smem_u32(&bars->c_empty[st]));
+        ptx::mbar_arrive(ptx::smem_u32(&bars->t_empty[buf]));
+      }
     }
     const int grow = row0 + i;
     if (ok && !*abort && i < rpt && grow < rows && bi != 0x7FFFFFFF)
@@ -335,10 +358,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) readout_tc_kernel(
   }
 }
 
-constexpr size_t smem_bytes(int kch) {
-  return 1024 + (size_t)kch * A_CHUNK_BYTES + W2_STAGES * W2_STAGE_BYTES +
-         BASE_STAGES * BASE_STAGE_BYTES + sizeof(Bars);
+constexpr size_t smem_bytes() {
+  return 1024 + (size_t)W2_STAGES * W2_STAGE_BYTES + BASE_STAGES * BASE_STAGE_BYTES + sizeof(Bars);
 }
+static_assert(smem_bytes() <= 227 * 1024, "readout shared memory");
 
 bool encode(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* dims,
             const cuuint64_t* strides, const cuuint32_t* box) {
@@ -388,14 +411,14 @@ int resident_ctas(size_t smem) {
 }
 
 template <int KCH, int MC>
-cudaError_t launch_mc(const xp_head* h, const CUtensorMap& tl, const CUtensorMap& tb, int N,
+cudaError_t launch_mc(const xp_head* h, const void* lat, const CUtensorMap& tb, int N,
                       int n_seg, int64_t* blk, float* win, unsigned long long* packed,
                       unsigned* ticket, cudaStream_t s) {
   const int Bm1 = h->B - 1, rows = N * Bm1;
   const int bpt = BM / Bm1, rpt = bpt * Bm1;
   const int n_rt = (N + bpt - 1) / bpt;
   const int nvt = (h->V + BN - 1) / BN;
-  const size_t smem = smem_bytes(KCH);
+  const size_t smem = smem_bytes();
   cudaError_t e = cudaFuncSetAttribute(readout_tc_kernel<KCH, MC>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
@@ -414,7 +437,8 @@ cudaError_t launch_mc(const xp_head* h, const CUtensorMap& tl, const CUtensorMap
   cfg.attrs = attr;
   cfg.numAttrs = MC > 1 ? 2 : 1;
   const CUtensorMap& tw = MC == 1 ? h->tm_w2 : h->tm_w2_slice[MC == 2 ? 0 : 1];
-  e = cudaLaunchKernelEx(&cfg, readout_tc_kernel<KCH, MC>, tl, tw, tb, rows, Bm1, h->B, h->V, rpt,
+  e = cudaLaunchKernelEx(&cfg, readout_tc_kernel<KCH, MC>, (const __nv_bfloat16*)lat, tw, tb,
+                         rows, Bm1, h->B, h->V, rpt,
                          bpt, n_rt, n_seg, nvt, blk, win,
                          h->latent_mma ? (const float*)h->E : (const float*)nullptr, h->r * 4,
                          packed, ticket, h->err);
@@ -425,26 +449,26 @@ cudaError_t launch_mc(const xp_head* h, const CUtensorMap& tl, const CUtensorMap
 // w2 chunk by multicast; MC is the largest of 4, 2 that divides the row tiles and lets
 // the launch fill at least as many SMs as 7/8 of the plain launch, else 1.
 template <int KCH>
-cudaError_t launch(const xp_head* h, const CUtensorMap& tl, const CUtensorMap& tb, int N,
+cudaError_t launch(const xp_head* h, const void* lat, const CUtensorMap& tb, int N,
                    int64_t* blk, float* win, unsigned long long* packed, unsigned* ticket,
                    cudaStream_t s) {
   const int bpt = BM / (h->B - 1);
   const int n_rt = (N + bpt - 1) / bpt;
   const int nvt = (h->V + BN - 1) / BN;
-  const size_t smem = smem_bytes(KCH);
+  const size_t smem = smem_bytes();
   auto segs = [&](int resident) { return std::min(nvt, resident / n_rt); };
   const int seg1 = std::max(1, std::min(nvt, h->num_sms / n_rt));
   if (h->readout_mc && n_rt % 4 == 0) {
     const int sg = segs(resident_ctas<KCH, 4>(smem));
     if (sg >= 1 && 8 * sg >= 7 * seg1)
-      return launch_mc<KCH, 4>(h, tl, tb, N, sg, blk, win, packed, ticket, s);
+      return launch_mc<KCH, 4>(h, lat, tb, N, sg, blk, win, packed, ticket, s);
   }
   if (h->readout_mc && n_rt % 2 == 0) {
     const int sg = segs(resident_ctas<KCH, 2>(smem));
     if (sg >= 1 && 8 * sg >= 7 * seg1)
-      return launch_mc<KCH, 2>(h, tl, tb, N, sg, blk, win, packed, ticket, s);
+      return launch_mc<KCH, 2>(h, lat, tb, N, sg, blk, win, packed, ticket, s);
   }
-  return launch_mc<KCH, 1>(h, tl, tb, N, seg1, blk, win, packed, ticket, s);
+  return launch_mc<KCH, 1>(h, lat, tb, N, seg1, blk, win, packed, ticket, s);
 }
 
 }  // namespace
@@ -463,13 +487,7 @@ cudaError_t xp_launch_readout_tc(const xp_head* h, const void* lat, const void* 
   if (!xp_readout_tc_call_ok(h, lat, base, sn, sb, N)) return cudaErrorNotSupported;
   const int Bm1 = h->B - 1;
   const int bpt = BM / Bm1;
-  CUtensorMap tl, tb;
-  {
-    const cuuint64_t dims[2] = {(cuuint64_t)h->r, (cuuint64_t)N * Bm1};
-    const cuuint64_t strides[1] = {(cuuint64_t)h->r * 2};
-    const cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)BM};
-    if (!encode(&tl, lat, 2, dims, strides, box)) return cudaErrorNotSupported;
-  }
+  CUtensorMap tb;
   {
     const cuuint64_t dims[3] = {(cuuint64_t)h->V, (cuuint64_t)Bm1, (cuuint64_t)N};
     const cuuint64_t strides[2] = {(cuuint64_t)sb * 2, (cuuint64_t)sn * 2};
@@ -477,10 +495,10 @@ cudaError_t xp_launch_readout_tc(const xp_head* h, const void* lat, const void* 
     if (!encode(&tb, base, 3, dims, strides, box)) return cudaErrorNotSupported;
   }
   switch (h->r / BK) {
-    case 1: return launch<1>(h, tl, tb, N, blk, win, packed, ticket, s);
-    case 2: return launch<2>(h, tl, tb, N, blk, win, packed, ticket, s);
-    case 3: return launch<3>(h, tl, tb, N, blk, win, packed, ticket, s);
-    case 4: return launch<4>(h, tl, tb, N, blk, win, packed, ticket, s);
+    case 1: return launch<1>(h, lat, tb, N, blk, win, packed, ticket, s);
+    case 2: return launch<2>(h, lat, tb, N, blk, win, packed, ticket, s);
+    case 3: return launch<3>(h, lat, tb, N, blk, win, packed, ticket, s);
+    case 4: return launch<4>(h, lat, tb, N, blk, win, packed, ticket, s);
   }
   return cudaErrorNotSupported;
 }
