@@ -128,11 +128,15 @@ __global__ void __launch_bounds__(256) init_argmax_kernel(
     if (win) win[row] = packed_val(pk);
     if (b == 0 && anchor) blk[(int64_t)n * B] = checked_token(anchor[n], V, err);
   }
+  // launched to overlap an independent predecessor: finish only after it has, so that
+  // the kernels after this one see its results too (a no-op without the dependency)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 cudaError_t xp_launch_init_argmax(const xp_head* h, const void* base, int64_t sn, int64_t sb,
                                   const int64_t* anchor, int N, int64_t* blk, float* win,
-                                  unsigned long long* packed, unsigned* ticket, cudaStream_t s) {
+                                  unsigned long long* packed, unsigned* ticket, cudaStream_t s,
+                                  bool overlap_prev) {
   const int Bm1 = h->B - 1, rows = N * Bm1, V = h->V;
   const size_t es = xp_elem(h->dtype);
   const int E = (int)(16 / es);
@@ -146,8 +150,14 @@ cudaError_t xp_launch_init_argmax(const xp_head* h, const void* base, int64_t sn
   splits = (V + vchunk - 1) / vchunk;
   dim3 grid(splits, rows);
 #define XP_INIT_LAUNCH(T, VEC)                                                                  \
-  init_argmax_kernel<T, VEC><<<grid, 256, 0, s>>>((const T*)base, sn, sb, Bm1, h->B, V, vchunk, \
-                                                  anchor, blk, win, packed, ticket, h->err)
+  do {                                                                                          \
+    if (overlap_prev)                                                                           \
+      return xp_launch_pdl(init_argmax_kernel<T, VEC>, grid, dim3(256), 0, s, (const T*)base, sn, \
+                           sb, Bm1, h->B, V, vchunk, anchor, blk, win, packed, ticket, h->err);  \
+    init_argmax_kernel<T, VEC><<<grid, 256, 0, s>>>((const T*)base, sn, sb, Bm1, h->B, V,       \
+                                                    vchunk, anchor, blk, win, packed, ticket,   \
+                                                    h->err);                                    \
+  } while (0)
   if (h->dtype == XP_BF16) {
     if (vec) XP_INIT_LAUNCH(bf16, true); else XP_INIT_LAUNCH(bf16, false);
   } else {

@@ -105,6 +105,7 @@ __global__ void __launch_bounds__(THREADS, 1) hidden_tc_kernel(
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
+  ptx::pdl_trigger();           // a launch that depends on nothing here may start now
 
   if (warp == 0) {
     if (lane == 0) {
@@ -200,6 +201,7 @@ __global__ void __launch_bounds__(256) xh_reduce_kernel(const float* __restrict_
                                                         float* __restrict__ xh, int B, int r) {
   __shared__ float red[8][32];
   const int tx = threadIdx.x, ty = threadIdx.y;
+  ptx::pdl_wait();              // the partials come from an earlier kernel
   const int c = blockIdx.x * 32 + tx, n = blockIdx.y;
   const int two_r = 2 * r;
   float gsum = 0.f;
@@ -263,8 +265,8 @@ bool xp_hidden_tc_call_ok(const xp_head* h, const void* h_full) {
   return h->hidden_tc && (uintptr_t)h_full % 16 == 0;
 }
 
-cudaError_t xp_launch_hidden_tc(const xp_head* h, const void* h_full, int N, float* xh,
-                                float* part, int part_rows, cudaStream_t s) {
+cudaError_t xp_launch_hidden_tc_gemm(const xp_head* h, const void* h_full, int N, float* part,
+                                     int part_rows, cudaStream_t s, int* splits_out) {
   const int rows = N * h->B, two_r = 2 * h->r;
   CUtensorMap tm_h;
   if (!encode_bf16_2d(&tm_h, h_full, (uint64_t)h->hidden, (uint64_t)rows, HK, HM))
@@ -279,9 +281,23 @@ cudaError_t xp_launch_hidden_tc(const xp_head* h, const void* h_full, int N, flo
   const int64_t stride = (int64_t)rows * two_r;
   hidden_tc_kernel<<<dim3(n_tiles, m_tiles, splits), THREADS, kSmem, s>>>(
       tm_h, h->tm_hfold, rows, two_r, nkb, splits, part, stride, h->err);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  xh_reduce_kernel<<<dim3((h->r + 31) / 32, N), dim3(32, 8), 0, s>>>(part, stride, splits, xh,
-                                                                     h->B, h->r);
+  *splits_out = splits;
   return cudaGetLastError();
+}
+
+cudaError_t xp_launch_xh_reduce(const xp_head* h, int N, float* xh, const float* part, int splits,
+                                cudaStream_t s, bool pdl) {
+  const int64_t stride = (int64_t)N * h->B * 2 * h->r;
+  const dim3 grid((h->r + 31) / 32, N), block(32, 8);
+  if (pdl) return xp_launch_pdl(xh_reduce_kernel, grid, block, 0, s, part, stride, splits, xh, h->B, h->r);
+  xh_reduce_kernel<<<grid, block, 0, s>>>(part, stride, splits, xh, h->B, h->r);
+  return cudaGetLastError();
+}
+
+cudaError_t xp_launch_hidden_tc(const xp_head* h, const void* h_full, int N, float* xh,
+                                float* part, int part_rows, cudaStream_t s) {
+  int splits = 0;
+  const cudaError_t e = xp_launch_hidden_tc_gemm(h, h_full, N, part, part_rows, s, &splits);
+  if (e != cudaSuccess) return e;
+  return xp_launch_xh_reduce(h, N, xh, part, splits, s, false);
 }

@@ -313,8 +313,30 @@ xp_status xp_jacobi_refine(const xp_head* h, const void* base, int64_t sn, int64
   char* w = (char*)ws;
   float* xh = (float*)(w + L.xh);
   void* lat = w + L.lat;
-  xp_status st = cuda_status(xp_launch_hidden(h, h_full, N, xh, (float*)(w + L.part),
-                                              (float*)(w + L.hc), L.part_rows, stream));
+  xp_status st = XP_OK;
+  if (C == 0 && xp_hidden_tc_call_ok(h, h_full)) {
+    // the hidden-cache GEMM and the init argmax are independent: the init runs beside
+    // the GEMM, the reduce of the GEMM's partials after both
+    int splits = 0;
+    cudaError_t e = xp_launch_hidden_tc_gemm(h, h_full, N, (float*)(w + L.part), L.part_rows,
+                                             stream, &splits);
+    if (e == cudaSuccess)
+      e = xp_launch_init_argmax(h, base, sn, sb, anchor, N, blk, nullptr,
+                                (unsigned long long*)(w + L.in_packed),
+                                (unsigned*)(w + L.in_ticket), stream, true);
+    if (e == cudaSuccess) e = xp_launch_xh_reduce(h, N, xh, (float*)(w + L.part), splits, stream, true);
+    if (e != cudaErrorNotSupported) {
+      st = cuda_status(e);
+      for (int k = 0; k < K && st == XP_OK; ++k) {
+        st = xp_latent_pass(h, blk, am1, xh, N, lat, stream);
+        if (st == XP_OK) st = readout_impl(h, lat, base, sn, sb, N, blk, nullptr, ws, stream);
+      }
+      return st;
+    }
+    cudaGetLastError();   // nothing was launched: take the general path below
+  }
+  st = cuda_status(xp_launch_hidden(h, h_full, N, xh, (float*)(w + L.part), (float*)(w + L.hc),
+                                    L.part_rows, stream));
   if (st != XP_OK) return st;
   if (C == 0) {
     st = cuda_status(xp_launch_init_argmax(h, base, sn, sb, anchor, N, blk, nullptr,

@@ -67,10 +67,21 @@ bool xp_hidden_tc_call_ok(const xp_head* h, const void* h_full);
 // returns cudaErrorNotSupported when h_full cannot be tiled by TMA
 cudaError_t xp_launch_hidden_tc(const xp_head* h, const void* h_full, int N, float* xh,
                                 float* part, int part_rows, cudaStream_t s);
+// the same in two launches, so that independent work can run between them: the GEMM
+// lets a programmatically dependent launch start early; the reduce (pdl = true) waits
+// for its predecessor before reading the partials
+cudaError_t xp_launch_hidden_tc_gemm(const xp_head* h, const void* h_full, int N, float* part,
+                                     int part_rows, cudaStream_t s, int* splits_out);
+cudaError_t xp_launch_xh_reduce(const xp_head* h, int N, float* xh, const float* part, int splits,
+                                cudaStream_t s, bool pdl);
 
+// overlap_prev: launch with a programmatic dependency on the previous kernel, which
+// must touch none of base, blk, win or the argmax scratch; the kernel waits for that
+// kernel only at its end, so whatever follows sees both completed
 cudaError_t xp_launch_init_argmax(const xp_head* h, const void* base, int64_t sn, int64_t sb,
                                   const int64_t* anchor, int N, int64_t* blk, float* win,
-                                  unsigned long long* packed, unsigned* ticket, cudaStream_t s);
+                                  unsigned long long* packed, unsigned* ticket, cudaStream_t s,
+                                  bool overlap_prev = false);
 
 cudaError_t xp_launch_latent_simt(const xp_head* h, const int64_t* blk, const int64_t* am1,
                                   const float* xh, int N, void* lat, cudaStream_t s);
