@@ -296,7 +296,15 @@ def other_workloads(args):
             nbytes = rows * C * wl.r * 2 + rows * C * 2 + rows * C * 8 + rows * wl.r * 2 + rows * 8
             r["topc_readout"] = {"us": round(us, 2), "algorithmic_bytes": nbytes,
                                  "achieved_gbs": round(nbytes / us / 1e3, 1),
-                                 "frac_of_hbm": round(nbytes / us / 1e3 / hbm, 4)}
+                                 "frac_of_hbm": round(nbytes / us / 1e3 / hbm, 4),
+                                 "w2_rows": "copied once per step (w2c)"}
+            # the same pass reading the candidates' rows by id from w2 (L2-resident)
+            t0.record(stream)
+            for _ in range(n):
+                xp.xp_topc_readout_argmax(head.handle, lat, base_c, cand, None, wl.N, C, blk, None)
+            t1.record(stream)
+            torch.cuda.synchronize()
+            r["topc_readout_by_id_us"] = round(t0.elapsed_time(t1) / n * 1e3, 2)
             r["topc_gather_us"] = round(g0.elapsed_time(g1) * 1e3, 1)
             del cand, base_c, w2c, lat
         res[name] = r

@@ -194,6 +194,9 @@ xp_status xp_topc_readout_argmax(const xp_head* head, const void* lat, const voi
  * then K passes of latent + readout-argmax.  blk: device [N, B] int64 (out;
  * slot 0 = anchor).  topc >= V scores the full vocabulary through the top-C
  * path with C = V.  ws: workspace of xp_workspace_bytes(w, >= N, topc).
+ * Top-C: the candidates' w2 rows are copied once per step while N*(B-1)*C <= V
+ * (the copy is no larger than w2); for larger batches every pass reads them by id
+ * from w2 instead.  Both give the same blk.
  * qwen3_xpress page, XPressRefinerHead.jacobi_refine_greedy. */
 xp_status xp_jacobi_refine(const xp_head* head, const void* base, int64_t stride_n,
                            int64_t stride_b, const void* h_full, const int64_t* anchor,

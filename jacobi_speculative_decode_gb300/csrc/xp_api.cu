@@ -350,7 +350,10 @@ xp_status xp_jacobi_refine(const xp_head* h, const void* base, int64_t sn, int64
   }
   int64_t* cand = (int64_t*)(w + L.cand);
   void* base_c = w + L.base_c;
-  void* w2c = w + L.w2c;
+  // the candidates' w2 rows are copied out once per step only while they take less room
+  // than w2 itself; beyond that every pass reads them by id from w2, which then stays
+  // resident in L2, instead of streaming the larger copy from HBM
+  void* w2c = (int64_t)N * (h->B - 1) * C <= (int64_t)h->V ? (void*)(w + L.w2c) : nullptr;
   st = cuda_status(
       xp_launch_topc_gather(h, base, sn, sb, N, C, cand, base_c, w2c, blk, anchor, stream));
   for (int k = 0; k < K && st == XP_OK; ++k) {
