@@ -355,9 +355,14 @@ def breakdown(wl, head, base, sn, sb, h, anchor, am1, ws, stream, rank):
     ro_ms = loop_us(readout)
     lat_ms = loop_us(latent)
     pass_ms = loop_us(one_pass)
+    # the unfused readout: the same rows' fp32 logits written out instead of their argmax
+    out = torch.empty(rows, wl.V, dtype=torch.float32, device="cuda")
+    lg_ms = loop_us(lambda: xp.xp_refine_logits(head.handle, lat, base, sn, sb, wl.N, out, wl.V))
+    del out
     # algorithmic bytes of one readout launch: w2 + base rows + latents in + blk out
     es = 2 if wl.dtype == "bf16" else 4
     ro_bytes = wl.V * wl.r * es + rows * wl.V * es + rows * wl.r * es + rows * 8
+    lg_bytes = wl.V * wl.r * es + rows * wl.V * es + rows * wl.r * es + rows * wl.V * 4
     hbm, kind = peaks()
     achieved = ro_bytes / (ro_ms / 1e3) / 1e9
     traffic = committed_traffic(rows)
@@ -369,6 +374,10 @@ def breakdown(wl, head, base, sn, sb, h, anchor, am1, ws, stream, rank):
                      "peak_kind": f"{kind} (copy bandwidth, burst)"},
         "kernel_us": {"readout_argmax": round(ro_ms * 1e3, 2), "latent": round(lat_ms * 1e3, 2),
                       "pass": round(pass_ms * 1e3, 2)},
+        # w2 + base rows + latents in, rows x V fp32 logits out
+        "refine_logits": {"us": round(lg_ms * 1e3, 2), "bytes": lg_bytes,
+                          "achieved_gbs": round(lg_bytes / (lg_ms / 1e3) / 1e9, 1),
+                          "frac": round(lg_bytes / (lg_ms / 1e3) / 1e9 / hbm, 4)},
         # what the latent stage adds to a pass: pass time minus the readout's own time
         "latent_share_of_pass": round(max(pass_ms - ro_ms, 0.0) / pass_ms, 4),
     }

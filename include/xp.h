@@ -147,6 +147,23 @@ xp_status xp_readout_argmax(const xp_head* head, const void* lat, const void* ba
                             int64_t stride_n, int64_t stride_b, int N, int64_t* blk,
                             float* win_val, void* ws, cudaStream_t stream);
 
+/* Unfused readout: the draft rows' logits (or the refiner bias alone) instead of
+ * their argmax, for callers that sample or otherwise need the distribution:
+ *   out[n*(B-1) + b, v] = base[n,b,v] + lat[n,b] . w2[v]   (base given)
+ *   out[n*(B-1) + b, v] = lat[n,b] . w2[v]                 (base == NULL)
+ * for b = 0..B-2 (the draft slots 1..B-1; slot 0 holds the anchor, whose bias
+ * the method never reads).  lat and base as for xp_readout_argmax; base may be
+ * NULL.  out: device fp32, row r of the N*(B-1) rows at out + r*ld_out, ld_out
+ * >= V elements; the caller owns it (N*(B-1)*ld_out*4 bytes).  Products are
+ * accumulated in fp32 and the base value is added in fp32: out is the exact
+ * logit up to fp32 rounding, not rounded to the head dtype.  No workspace.
+ * XP_EINVAL: null lat/out, ld_out < V, negative N or strides.
+ * qwen3_xpress page, refine_bias (w2 applied to the refined latent) and the
+ * base + bias sum that fused_add_argmax_to_blk reduces. */
+xp_status xp_refine_logits(const xp_head* head, const void* lat, const void* base,
+                           int64_t stride_n, int64_t stride_b, int N, float* out,
+                           int64_t ld_out, cudaStream_t stream);
+
 /* xp_readout_argmax for callers that cannot allocate device memory -- no
  * counterpart on the pages; the refinement method itself says nothing about
  * where scratch lives.  Same arguments and results as xp_readout_argmax,

@@ -262,15 +262,17 @@ cudaError_t xp_launch_latent_simt(const xp_head* h, const int64_t* blk, const in
 // SIMT readout + argmax (xpress kernels page, fused_add_argmax_to_blk, with
 // the w2 matmul fused in): tile of 32 rows x 128 vocabulary ids, fp32 FMA.
 // The logits live in registers only; per-row (max, id) partials merge with
-// atomicMax and the last CTA of a row tile writes blk.
+// atomicMax and the last CTA of a row tile writes blk.  EMIT: the same tile writes
+// the fp32 logits (the bias alone when base is null) instead.
 // ---------------------------------------------------------------------------
 constexpr int SR_RT = 32, SR_VT = 128, SR_KC = 32;
 
-template <typename T>
+template <typename T, bool EMIT>
 __global__ void __launch_bounds__(256) readout_simt_kernel(
     const T* __restrict__ lat, const T* __restrict__ base, int64_t sn, int64_t sb,
     const T* __restrict__ w2, int rows, int Bm1, int B, int V, int r, int64_t* __restrict__ blk,
-    float* __restrict__ win, unsigned long long* __restrict__ packed, unsigned* __restrict__ ticket) {
+    float* __restrict__ win, unsigned long long* __restrict__ packed, unsigned* __restrict__ ticket,
+    float* __restrict__ out, int64_t ldo) {
   __shared__ float Ls[SR_KC][SR_RT];
   __shared__ float Ws[SR_KC][SR_VT + 1];
   __shared__ int s_last;
@@ -306,6 +308,21 @@ __global__ void __launch_bounds__(256) readout_simt_kernel(
         for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], bb[j], acc[i][j]);
     }
     __syncthreads();
+  }
+  if constexpr (EMIT) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int row = row0 + w * 4 + i;
+      if (row >= rows) continue;
+      const int n = row / Bm1, b = row % Bm1;
+      const T* bp = base ? base + (int64_t)n * sn + (int64_t)b * sb : nullptr;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int v = v0 + l + 32 * j;
+        if (v < V) out[(int64_t)row * ldo + v] = acc[i][j] + (bp ? to_f(bp[v]) : 0.f);
+      }
+    }
+    return;
   }
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -347,12 +364,27 @@ cudaError_t xp_launch_readout_simt(const xp_head* h, const void* lat, const void
   const int Bm1 = h->B - 1, rows = N * Bm1;
   dim3 grid((h->V + SR_VT - 1) / SR_VT, (rows + SR_RT - 1) / SR_RT);
   if (h->dtype == XP_BF16)
-    readout_simt_kernel<bf16><<<grid, 256, 0, s>>>((const bf16*)lat, (const bf16*)base, sn, sb,
-                                                   (const bf16*)h->w2, rows, Bm1, h->B, h->V, h->r,
-                                                   blk, win, packed, ticket);
+    readout_simt_kernel<bf16, false><<<grid, 256, 0, s>>>(
+        (const bf16*)lat, (const bf16*)base, sn, sb, (const bf16*)h->w2, rows, Bm1, h->B, h->V,
+        h->r, blk, win, packed, ticket, nullptr, 0);
   else
-    readout_simt_kernel<float><<<grid, 256, 0, s>>>((const float*)lat, (const float*)base, sn, sb,
-                                                    (const float*)h->w2, rows, Bm1, h->B, h->V,
-                                                    h->r, blk, win, packed, ticket);
+    readout_simt_kernel<float, false><<<grid, 256, 0, s>>>(
+        (const float*)lat, (const float*)base, sn, sb, (const float*)h->w2, rows, Bm1, h->B, h->V,
+        h->r, blk, win, packed, ticket, nullptr, 0);
+  return cudaGetLastError();
+}
+
+cudaError_t xp_launch_logits_simt(const xp_head* h, const void* lat, const void* base, int64_t sn,
+                                  int64_t sb, int N, float* out, int64_t ldo, cudaStream_t s) {
+  const int Bm1 = h->B - 1, rows = N * Bm1;
+  dim3 grid((h->V + SR_VT - 1) / SR_VT, (rows + SR_RT - 1) / SR_RT);
+  if (h->dtype == XP_BF16)
+    readout_simt_kernel<bf16, true><<<grid, 256, 0, s>>>(
+        (const bf16*)lat, (const bf16*)base, sn, sb, (const bf16*)h->w2, rows, Bm1, h->B, h->V,
+        h->r, nullptr, nullptr, nullptr, nullptr, out, ldo);
+  else
+    readout_simt_kernel<float, true><<<grid, 256, 0, s>>>(
+        (const float*)lat, (const float*)base, sn, sb, (const float*)h->w2, rows, Bm1, h->B, h->V,
+        h->r, nullptr, nullptr, nullptr, nullptr, out, ldo);
   return cudaGetLastError();
 }

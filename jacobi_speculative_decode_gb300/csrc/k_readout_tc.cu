@@ -5,9 +5,11 @@
 // contiguous range of 192-wide vocabulary tiles.  The latent tile (128 rows x r)
 // lives in tensor memory as the MMA's A operand, so shared memory holds only the
 // two streams.  Per vocabulary tile:
-//   TMA   w2[v-tile, k-chunk]  (192 x 64 bf16, 128B-swizzled)  -> 5-stage smem ring
-//   TMA   base[rows, 64 ids]   (one box per 64-id third)        -> 6-stage smem ring
-//         (two tiles: the next tile's base is in flight while this one is reduced)
+//   TMA   w2[v-tile, k-chunk]  (192 x 64 bf16, 128B-swizzled)  -> 6-stage smem ring
+//   TMA   base[rows, 64 ids]   (one box per 64-id third)        -> 3-stage smem ring
+//         (one tile; each thread lifts its row's part of a stage into registers as
+//         soon as the tile before it has been reduced, which frees the stage for the
+//         next tile's base one tile earlier)
 //   MMA   tcgen05 M=128 (rows) x N=192 (vocab) x K=r, A from TMEM, fp32 accumulators
 //         in TMEM, double-buffered (2 x 192 columns; A takes the last 128 columns)
 //   epilogue: each thread owns one row (one TMEM lane), adds base, keeps a
@@ -37,19 +39,29 @@ constexpr int BM = 128;           // rows per MMA (TMEM lanes)
 constexpr int BN = 192;           // vocabulary ids per tile (MMA N)
 constexpr int BK = 64;            // k per swizzled chunk (128 bytes of bf16)
 constexpr int QPT = BN / 64;      // 64-id thirds per tile
-constexpr int W2_STAGES = 5;      // k-chunks of w2 in flight
-constexpr int BASE_STAGES = 2 * QPT;  // two tiles of base in flight; stage s always holds
-                                      // third s % QPT, so each has a single consumer group
+constexpr int BASE_STAGES = QPT;  // one tile of base in smem (one more is lifted into
+                                  // registers); stage s always holds third s, so each
+                                  // stage has a single consumer group
 constexpr int EPI_WARPS = 4 * QPT;                  // one warp per (lane quadrant, third)
 constexpr int W2_STAGE_BYTES = BN * BK * 2;         // 24 KB
 constexpr int BASE_STAGE_BYTES = 128 * 64 * 2;      // 16 KB: one 64-wide box of <= 128 rows
 constexpr int NUM_THREADS = (3 + EPI_WARPS) * 32;   // 480
+constexpr int OUT_STAGE_BYTES = 32 * 32 * 4;        // logits: one warp's 32 rows x 32 ids
+
+// k-chunks of w2 in flight: the argmax kernel spends all of shared memory on its rings;
+// the logits kernel gives part of it to the per-warp staging of its output.
+template <bool EMIT>
+struct Smem {
+  static constexpr int W2_STAGES = EMIT ? 4 : 6;
+  static constexpr int OUT_BYTES = EMIT ? EPI_WARPS * OUT_STAGE_BYTES : 0;
+};
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t A_COL = 2 * BN;                  // latent tile: columns [384, 384 + r/2)
 constexpr uint32_t IDESC = ptx::idesc_bf16_f32(BM, BN);
 static_assert(A_COL + 128 <= TMEM_COLS, "accumulators and the latent tile share TMEM");
 static_assert(BASE_STAGES % QPT == 0, "a base stage always holds the same third");
 
+template <int W2_STAGES>
 struct Bars {
   uint64_t a_full;
   uint64_t w_full[W2_STAGES], w_empty[W2_STAGES];
@@ -59,29 +71,38 @@ struct Bars {
   uint32_t tmem_base;
   int abort;
   int last;
+  uint32_t sink;      // see lift() in the epilogue
 };
 
 __device__ __forceinline__ float bf16lo(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
 
+// EMIT: instead of the argmax, write the logits base + lat.w2 (or the bias lat.w2 alone
+// when has_base is 0) as fp32 rows of `out`; every thread stages its row's 32 values of
+// a chunk in the warp's swizzled 4 KB buffer, and the warp then stores four full
+// 128-byte row segments per instruction.
+//
 // MC > 1: the kernel runs in clusters of MC CTAs, the MC row tiles of one vocabulary
 // segment.  Every w2 k-chunk is then loaded once per cluster: CTA c loads rows
 // [c * BN/MC, (c+1) * BN/MC) of it and multicasts them into the same stage of every
 // CTA, and a stage is refilled only after all MC MMA issuers released it (their
 // commits arrive on the stage's empty barrier in every CTA of the cluster).
-template <int KCH, int MC>
+template <int KCH, int MC, bool EMIT>
 __global__ void __launch_bounds__(NUM_THREADS, 1) readout_tc_kernel(
     const __nv_bfloat16* __restrict__ lat, const __grid_constant__ CUtensorMap tm_w2,
     const __grid_constant__ CUtensorMap tm_base, int rows, int Bm1, int B, int V, int rpt, int bpt,
     int n_rt, int n_seg, int nvt, int64_t* __restrict__ blk, float* __restrict__ win,
     const float* __restrict__ pf_rows, int pf_row_bytes,
-    unsigned long long* __restrict__ packed, unsigned* __restrict__ ticket, uint32_t* err) {
+    unsigned long long* __restrict__ packed, unsigned* __restrict__ ticket, uint32_t* err,
+    float* __restrict__ out, int64_t ldo, int has_base) {
+  constexpr int W2_STAGES = Smem<EMIT>::W2_STAGES;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = ptx::smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
   uint8_t* sW = smem;                                    // W2_STAGES x 24 KB
   uint8_t* sC = sW + W2_STAGES * W2_STAGE_BYTES;         // BASE_STAGES x 16 KB
-  Bars* bars = reinterpret_cast<Bars*>(sC + BASE_STAGES * BASE_STAGE_BYTES);
+  uint8_t* sO = sC + BASE_STAGES * BASE_STAGE_BYTES;    // EMIT: EPI_WARPS x 4 KB
+  auto* bars = reinterpret_cast<Bars<W2_STAGES>*>(sO + Smem<EMIT>::OUT_BYTES);
   volatile int* abort = &bars->abort;
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -125,7 +146,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) readout_tc_kernel(
 
   if (warp == 0) {
     // ---------------- base producer ----------------
-    if (lane == 0) {
+    if (lane == 0 && has_base) {
       ptx::prefetch_tmap(&tm_base);
       const uint64_t pol = ptx::policy_evict_first();
       const uint32_t box_bytes = 64u * (uint32_t)Bm1 * (uint32_t)bpt * 2u;
@@ -261,21 +282,42 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) readout_tc_kernel(
     }
     float best = -INFINITY;
     int bi = 0x7FFFFFFF;
-    int ti = 0;
-    bool ok = true;
-    for (int vt = vt0; vt < vt1 && ok; ++vt, ++ti) {
-      const int ci = ti * QPT + third;       // this third's fill index in the base ring
+    // This thread's 64 base values (its row, its third) of the tile about to be reduced.
+    // A base stage is lifted into registers and released as soon as the previous tile
+    // has been reduced, not after its own tile: the ring then keeps one more tile in
+    // flight than it holds.
+    uint4 bq[8] = {};
+    auto lift = [&](int ci) -> bool {
       const int st = ci % BASE_STAGES;
+      bool got = ptx::mbar_wait(ptx::smem_u32(&bars->c_full[st]), (ci / BASE_STAGES) & 1, abort, err);
+      got = __all_sync(0xFFFFFFFFu, got);
+      if (!got) return false;
+      const uint8_t* rowp = sC + st * BASE_STAGE_BYTES + i * 128;
+#pragma unroll
+      for (int lc = 0; lc < 8; ++lc)          // logical 16-byte chunk lc sits at lc ^ (row & 7)
+        bq[lc] = *reinterpret_cast<const uint4*>(rowp + ((lc ^ (i & 7)) << 4));
+      // The release lets TMA overwrite the stage at once, and a shared-memory load that
+      // has been issued but has not returned its data can still read it then: on this
+      // GPU the last chunks of a row came back as the next tile's base.  So the release
+      // waits for the data itself: every lane folds all of it into one word and stores
+      // that word, an instruction that cannot issue before every load has returned.
+      uint32_t dep = 0;
+#pragma unroll
+      for (int lc = 0; lc < 8; ++lc) dep ^= bq[lc].x ^ bq[lc].y ^ bq[lc].z ^ bq[lc].w;
+      asm volatile("st.shared.u32 [%0], %1;" ::"r"(ptx::smem_u32(&bars->sink)), "r"(dep) : "memory");
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->c_empty[st]));
+      return true;
+    };
+    bool ok = vt0 < vt1 && has_base ? lift(third) : true;
+    int ti = 0;
+    for (int vt = vt0; vt < vt1 && ok; ++vt, ++ti) {
       const int buf = ti & 1;
       ok = ptx::mbar_wait(ptx::smem_u32(&bars->t_full[buf]), (ti >> 1) & 1, abort, err);
       ok = __all_sync(0xFFFFFFFFu, ok);      // warp-uniform: tcgen05.ld is .sync.aligned
       if (!ok) break;
       ptx::tc_fence_after();
       const int vbase = vt * BN;
-      ok = ptx::mbar_wait(ptx::smem_u32(&bars->c_full[st]), (ci / BASE_STAGES) & 1, abort, err);
-      ok = __all_sync(0xFFFFFFFFu, ok);
-      if (!ok) break;
-      const uint8_t* rowp = sC + st * BASE_STAGE_BYTES + i * 128;
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
         const int col = third * 64 + cc * 32;
@@ -285,14 +327,42 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) readout_tc_kernel(
         float sc[32];
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch) {
-          const int lc = cc * 4 + ch;                // logical 16-byte chunk in the 128-byte row
-          const uint4 bv = *reinterpret_cast<const uint4*>(rowp + ((lc ^ (i & 7)) << 4));
+          const uint4 bv = bq[cc * 4 + ch];
           const uint32_t w4[4] = {bv.x, bv.y, bv.z, bv.w};
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             const float bval = (e & 1) ? bf16hi(w4[e >> 1]) : bf16lo(w4[e >> 1]);
             sc[ch * 8 + e] = __uint_as_float(acc[ch * 8 + e]) + bval;
           }
+        }
+        if constexpr (EMIT) {
+          uint8_t* stg = sO + (warp - 3) * OUT_STAGE_BYTES;
+          // row `lane` of the warp's 32: eight 16-byte chunks, chunk c at c ^ (lane & 7)
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<float4*>(stg + lane * 128 + ((c ^ (lane & 7)) << 4)) =
+                make_float4(sc[4 * c], sc[4 * c + 1], sc[4 * c + 2], sc[4 * c + 3]);
+          __syncwarp();
+          const int c = lane & 7;
+          const int v0 = vbase + col + c * 4;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int rl = j * 4 + (lane >> 3);    // row within the warp's 32
+            const int it = g * 32 + rl;            // row within the tile
+            const float4 q = *reinterpret_cast<const float4*>(stg + rl * 128 + ((c ^ (rl & 7)) << 4));
+            if (it < rpt && row0 + it < rows && v0 < V) {
+              float* dst = out + (int64_t)(row0 + it) * ldo + v0;
+              if (v0 + 4 <= V) {
+                __stcs(reinterpret_cast<float4*>(dst), q);
+              } else {
+                dst[0] = q.x;
+                if (v0 + 1 < V) dst[1] = q.y;
+                if (v0 + 2 < V) dst[2] = q.z;
+              }
+            }
+          }
+          __syncwarp();                            // before the next chunk refills it
+          continue;
         }
         const int vlim = V - (vbase + col);          // ids at or past V are padding
         if (vlim < 32) {                             // warp-uniform: only the last tile
@@ -315,19 +385,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) readout_tc_kernel(
       }
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) {
-        ptx::mbar_arrive(ptx::smem_u32(&bars->c_empty[st]));
-        ptx::mbar_arrive(ptx::smem_u32(&bars->t_empty[buf]));
-      }
+      if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->t_empty[buf]));
+      if (vt + 1 < vt1 && has_base) ok = lift((ti + 1) * QPT + third);
     }
     const int grow = row0 + i;
-    if (ok && !*abort && i < rpt && grow < rows && bi != 0x7FFFFFFF)
+    if (!EMIT && ok && !*abort && i < rpt && grow < rows && bi != 0x7FFFFFFF)
       atomicMax(packed + grow, pack_best(best, (uint32_t)bi));
   }
 
   // ---------------- publish: the last CTA of this row tile writes blk ----------------
   ptx::pdl_wait();            // blk may still be read by the kernel this one overlapped
-  const bool last = arrive_last(ticket + tile, (unsigned)n_seg, &bars->last);
+  const bool last = !EMIT && arrive_last(ticket + tile, (unsigned)n_seg, &bars->last);
   if (last && threadIdx.x < BM) {
     const int grow = row0 + threadIdx.x;
     if (threadIdx.x < rpt && grow < rows) {
@@ -358,10 +426,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) readout_tc_kernel(
   }
 }
 
+template <bool EMIT>
 constexpr size_t smem_bytes() {
-  return 1024 + (size_t)W2_STAGES * W2_STAGE_BYTES + BASE_STAGES * BASE_STAGE_BYTES + sizeof(Bars);
+  return 1024 + (size_t)Smem<EMIT>::W2_STAGES * W2_STAGE_BYTES + BASE_STAGES * BASE_STAGE_BYTES +
+         Smem<EMIT>::OUT_BYTES + sizeof(Bars<Smem<EMIT>::W2_STAGES>);
 }
-static_assert(smem_bytes() <= 227 * 1024, "readout shared memory");
+static_assert(smem_bytes<false>() <= 227 * 1024, "readout shared memory");
+static_assert(smem_bytes<true>() <= 227 * 1024, "logits shared memory");
 
 bool encode(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* dims,
             const cuuint64_t* strides, const cuuint32_t* box) {
@@ -379,11 +450,11 @@ int resident_ctas(size_t smem) {
   static int cached = -1;
   if (cached >= 0) return cached;
   int n = 0;
-  if (cudaFuncSetAttribute(readout_tc_kernel<KCH, MC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(readout_tc_kernel<KCH, MC, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)smem) == cudaSuccess) {
     if (MC == 1) {
       int per_sm = 0, dev = 0, sms = 0;
-      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, readout_tc_kernel<KCH, MC>,
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, readout_tc_kernel<KCH, MC, false>,
                                                         NUM_THREADS, smem) == cudaSuccess &&
           cudaGetDevice(&dev) == cudaSuccess &&
           cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
@@ -401,7 +472,7 @@ int resident_ctas(size_t smem) {
       cfg.attrs = attr;
       cfg.numAttrs = 1;
       int clusters = 0;
-      if (cudaOccupancyMaxActiveClusters(&clusters, readout_tc_kernel<KCH, MC>, &cfg) == cudaSuccess)
+      if (cudaOccupancyMaxActiveClusters(&clusters, readout_tc_kernel<KCH, MC, false>, &cfg) == cudaSuccess)
         n = clusters * MC;
     }
   }
@@ -418,8 +489,8 @@ cudaError_t launch_mc(const xp_head* h, const void* lat, const CUtensorMap& tb, 
   const int bpt = BM / Bm1, rpt = bpt * Bm1;
   const int n_rt = (N + bpt - 1) / bpt;
   const int nvt = (h->V + BN - 1) / BN;
-  const size_t smem = smem_bytes();
-  cudaError_t e = cudaFuncSetAttribute(readout_tc_kernel<KCH, MC>,
+  const size_t smem = smem_bytes<false>();
+  cudaError_t e = cudaFuncSetAttribute(readout_tc_kernel<KCH, MC, false>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -437,11 +508,42 @@ cudaError_t launch_mc(const xp_head* h, const void* lat, const CUtensorMap& tb, 
   cfg.attrs = attr;
   cfg.numAttrs = MC > 1 ? 2 : 1;
   const CUtensorMap& tw = MC == 1 ? h->tm_w2 : h->tm_w2_slice[MC == 2 ? 0 : 1];
-  e = cudaLaunchKernelEx(&cfg, readout_tc_kernel<KCH, MC>, (const __nv_bfloat16*)lat, tw, tb,
+  e = cudaLaunchKernelEx(&cfg, readout_tc_kernel<KCH, MC, false>, (const __nv_bfloat16*)lat, tw, tb,
                          rows, Bm1, h->B, h->V, rpt,
                          bpt, n_rt, n_seg, nvt, blk, win,
                          h->latent_mma ? (const float*)h->E : (const float*)nullptr, h->r * 4,
-                         packed, ticket, h->err);
+                         packed, ticket, h->err, (float*)nullptr, (int64_t)0, 1);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+// Logits: row tiles x vocabulary segments as in the argmax launch, without clusters.
+template <int KCH>
+cudaError_t launch_logits(const xp_head* h, const void* lat, const CUtensorMap& tb, int has_base,
+                          int N, float* out, int64_t ldo, cudaStream_t s) {
+  const int Bm1 = h->B - 1, rows = N * Bm1;
+  const int bpt = BM / Bm1, rpt = bpt * Bm1;
+  const int n_rt = (N + bpt - 1) / bpt;
+  const int nvt = (h->V + BN - 1) / BN;
+  const int n_seg = std::max(1, std::min(nvt, h->num_sms / n_rt));
+  const size_t smem = smem_bytes<true>();
+  cudaError_t e = cudaFuncSetAttribute(readout_tc_kernel<KCH, 1, true>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(n_rt * n_seg);
+  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, readout_tc_kernel<KCH, 1, true>, (const __nv_bfloat16*)lat,
+                         h->tm_w2, tb, rows, Bm1, h->B, h->V, rpt, bpt, n_rt, n_seg, nvt,
+                         (int64_t*)nullptr, (float*)nullptr, (const float*)nullptr, 0,
+                         (unsigned long long*)nullptr, (unsigned*)nullptr, h->err, out, ldo,
+                         has_base);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
@@ -455,7 +557,7 @@ cudaError_t launch(const xp_head* h, const void* lat, const CUtensorMap& tb, int
   const int bpt = BM / (h->B - 1);
   const int n_rt = (N + bpt - 1) / bpt;
   const int nvt = (h->V + BN - 1) / BN;
-  const size_t smem = smem_bytes();
+  const size_t smem = smem_bytes<false>();
   auto segs = [&](int resident) { return std::min(nvt, resident / n_rt); };
   const int seg1 = std::max(1, std::min(nvt, h->num_sms / n_rt));
   if (h->readout_mc && n_rt % 4 == 0) {
@@ -499,6 +601,36 @@ cudaError_t xp_launch_readout_tc(const xp_head* h, const void* lat, const void* 
     case 2: return launch<2>(h, lat, tb, N, blk, win, packed, ticket, s);
     case 3: return launch<3>(h, lat, tb, N, blk, win, packed, ticket, s);
     case 4: return launch<4>(h, lat, tb, N, blk, win, packed, ticket, s);
+  }
+  return cudaErrorNotSupported;
+}
+
+bool xp_logits_tc_call_ok(const xp_head* h, const void* lat, const void* base, int64_t sn,
+                          int64_t sb, int N, const float* out, int64_t ldo) {
+  if (!h->readout_tc || N <= 0 || (uintptr_t)lat % 16 != 0 || (uintptr_t)out % 16 != 0 ||
+      ldo % 4 != 0)
+    return false;
+  return !base || xp_readout_tc_call_ok(h, lat, base, sn, sb, N);
+}
+
+cudaError_t xp_launch_logits_tc(const xp_head* h, const void* lat, const void* base, int64_t sn,
+                                int64_t sb, int N, float* out, int64_t ldo, cudaStream_t s) {
+  if (!xp_logits_tc_call_ok(h, lat, base, sn, sb, N, out, ldo)) return cudaErrorNotSupported;
+  const int Bm1 = h->B - 1;
+  const int bpt = BM / Bm1;
+  CUtensorMap tb = h->tm_w2;      // never read when there is no base
+  if (base) {
+    const cuuint64_t dims[3] = {(cuuint64_t)h->V, (cuuint64_t)Bm1, (cuuint64_t)N};
+    const cuuint64_t strides[2] = {(cuuint64_t)sb * 2, (cuuint64_t)sn * 2};
+    const cuuint32_t box[3] = {64, (cuuint32_t)Bm1, (cuuint32_t)bpt};
+    if (!encode(&tb, base, 3, dims, strides, box)) return cudaErrorNotSupported;
+  }
+  const int hb = base ? 1 : 0;
+  switch (h->r / BK) {
+    case 1: return launch_logits<1>(h, lat, tb, hb, N, out, ldo, s);
+    case 2: return launch_logits<2>(h, lat, tb, hb, N, out, ldo, s);
+    case 3: return launch_logits<3>(h, lat, tb, hb, N, out, ldo, s);
+    case 4: return launch_logits<4>(h, lat, tb, hb, N, out, ldo, s);
   }
   return cudaErrorNotSupported;
 }

@@ -263,6 +263,20 @@ xp_status xp_readout_argmax(const xp_head* h, const void* lat, const void* base,
   return readout_impl(h, lat, base, sn, sb, N, blk, win, ws, stream);
 }
 
+xp_status xp_refine_logits(const xp_head* h, const void* lat, const void* base, int64_t sn,
+                           int64_t sb, int N, float* out, int64_t ld_out, cudaStream_t stream) {
+  if (!h) return XP_ENOTPREPARED;
+  if (!lat || !out || (base && !valid_base(h, base, sn, sb)) || ld_out < h->V || N < 0)
+    return XP_EINVAL;
+  if (N > h->max_N) return XP_ECAPACITY;
+  if (N == 0) return XP_OK;
+  if (xp_logits_tc_call_ok(h, lat, base, sn, sb, N, out, ld_out)) {
+    const cudaError_t e = xp_launch_logits_tc(h, lat, base, sn, sb, N, out, ld_out, stream);
+    if (e != cudaErrorNotSupported) return cuda_status(e);
+  }
+  return cuda_status(xp_launch_logits_simt(h, lat, base, sn, sb, N, out, ld_out, stream));
+}
+
 xp_status xp_init_argmax(const xp_head* h, const void* base, int64_t sn, int64_t sb,
                          const int64_t* anchor, int N, int64_t* blk, float* win, void* ws,
                          cudaStream_t stream) {

@@ -103,6 +103,14 @@ cudaError_t xp_launch_readout_tc(const xp_head* h, const void* lat, const void* 
 int xp_readout_tc_tile();   // vocabulary ids per tile of the tcgen05 readout (w2 map box rows)
 bool xp_readout_tc_call_ok(const xp_head* h, const void* lat, const void* base, int64_t sn,
                            int64_t sb, int N);
+// logits base + lat.w2 (bias alone when base is null) as fp32 rows of out (row stride ldo)
+cudaError_t xp_launch_logits_simt(const xp_head* h, const void* lat, const void* base, int64_t sn,
+                                  int64_t sb, int N, float* out, int64_t ldo, cudaStream_t s);
+// returns cudaErrorNotSupported when the tcgen05 path cannot take the call
+cudaError_t xp_launch_logits_tc(const xp_head* h, const void* lat, const void* base, int64_t sn,
+                                int64_t sb, int N, float* out, int64_t ldo, cudaStream_t s);
+bool xp_logits_tc_call_ok(const xp_head* h, const void* lat, const void* base, int64_t sn,
+                          int64_t sb, int N, const float* out, int64_t ldo);
 
 cudaError_t xp_launch_topc_gather(const xp_head* h, const void* base, int64_t sn, int64_t sb,
                                   int N, int C, int64_t* cand, void* base_c, void* w2c,

@@ -54,6 +54,7 @@ _SIGS = {
     "xp_latent_pass": (_I, [_P, _P, _P, _P, _I, _P, _P]),
     "xp_readout_argmax": (_I, [_P, _P, _P, _I64, _I64, _I, _P, _P, _P, _P]),
     "xp_readout_argmax_noalloc": (_I, [_P, _P, _P, _I64, _I64, _I, _P, _P, _P]),
+    "xp_refine_logits": (_I, [_P, _P, _P, _I64, _I64, _I, _P, _I64, _P]),
     "xp_init_argmax": (_I, [_P, _P, _I64, _I64, _P, _I, _P, _P, _P, _P]),
     "xp_topc_gather": (_I, [_P, _P, _I64, _I64, _I, _I, _P, _P, _P, _P, _P]),
     "xp_topc_readout_argmax": (_I, [_P, _P, _P, _P, _P, _I, _I, _P, _P, _P]),
@@ -179,6 +180,12 @@ def xp_readout_argmax_noalloc(head, lat, base, stride_n, stride_b, N, blk, win_v
     _check("xp_readout_argmax_noalloc", lib().xp_readout_argmax_noalloc(
         head, _ptr(lat), _ptr(base), stride_n, stride_b, N, _ptr(blk), _ptr(win_val),
         _stream(stream)))
+
+
+def xp_refine_logits(head, lat, base, stride_n, stride_b, N, out, ld_out, stream=None):
+    """Draft rows' fp32 logits base + lat.w2 (the bias alone when base is None)."""
+    _check("xp_refine_logits", lib().xp_refine_logits(
+        head, _ptr(lat), _ptr(base), stride_n, stride_b, N, _ptr(out), ld_out, _stream(stream)))
 
 
 def xp_init_argmax(head, base, stride_n, stride_b, anchor, N, blk, win_val, ws, stream=None):
