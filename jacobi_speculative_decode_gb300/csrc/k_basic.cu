@@ -84,26 +84,49 @@ __global__ void __launch_bounds__(256) init_argmax_kernel(
   if (VEC) {
     constexpr int E = 16 / sizeof(T);
     const int nvec = (v1 - v0) / E;
-    constexpr int U = 4;                         // 16-byte loads in flight per thread
-    for (int i0 = threadIdx.x; i0 < nvec; i0 += U * blockDim.x) {
-      uint4 q[U];
+    constexpr int U = 4;                         // 16-byte loads per thread and batch
+    const uint4* src = reinterpret_cast<const uint4*>(p + v0);
+    const int stride = U * (int)blockDim.x;
+    // two batches in flight: the next batch is loaded before this one is reduced
+    uint4 q[U], qn[U];
+    auto load = [&](uint4 (&dst)[U], int i0) {
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        const int i = i0 + u * blockDim.x;
-        q[u] = i < nvec ? __ldcs(reinterpret_cast<const uint4*>(p + v0 + i * E))
-                        : make_uint4(0, 0, 0, 0);
+        const int i = i0 + u * (int)blockDim.x;
+        dst[u] = i < nvec ? __ldcs(src + i) : make_uint4(0, 0, 0, 0);
       }
+    };
+    load(q, threadIdx.x);
+    for (int i0 = threadIdx.x; i0 < nvec; i0 += stride) {
+      load(qn, i0 + stride);
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        const int i = i0 + u * blockDim.x;
+        const int i = i0 + u * (int)blockDim.x;
         if (i >= nvec) break;
         const T* e = reinterpret_cast<const T*>(&q[u]);
+        if constexpr (sizeof(T) == 2) {
+          // the chunk's maximum in packed bf16 first; its lowest index only when it wins
+          const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&q[u]);
+          const __nv_bfloat162 m2 = __hmax2(__hmax2(h2[0], h2[1]), __hmax2(h2[2], h2[3]));
+          const float m = fmaxf(__low2float(m2), __high2float(m2));
+          if (m > best) {
+            int first = E - 1;
 #pragma unroll
-        for (int k = 0; k < E; ++k) {
-          const float x = to_f(e[k]);
-          if (x > best) { best = x; bi = v0 + i * E + k; }
+            for (int k = E - 1; k >= 0; --k)
+              if (to_f(e[k]) == m) first = k;
+            best = m;
+            bi = v0 + i * E + first;
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < E; ++k) {
+            const float x = to_f(e[k]);
+            if (x > best) { best = x; bi = v0 + i * E + k; }
+          }
         }
       }
+#pragma unroll
+      for (int u = 0; u < U; ++u) q[u] = qn[u];
     }
     vtail = v0 + nvec * E;
   }
@@ -322,39 +345,39 @@ __global__ void __launch_bounds__(256) readout_simt_kernel(
         if (v < V) out[(int64_t)row * ldo + v] = acc[i][j] + (bp ? to_f(bp[v]) : 0.f);
       }
     }
-    return;
-  }
+  } else {
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int row = row0 + w * 4 + i;
-    float best = -INFINITY;
-    int bi = 0x7FFFFFFF;
-    if (row < rows) {
-      const int n = row / Bm1, b = row % Bm1;
-      const T* bp = base + (int64_t)n * sn + (int64_t)b * sb;
+    for (int i = 0; i < 4; ++i) {
+      const int row = row0 + w * 4 + i;
+      float best = -INFINITY;
+      int bi = 0x7FFFFFFF;
+      if (row < rows) {
+        const int n = row / Bm1, b = row % Bm1;
+        const T* bp = base + (int64_t)n * sn + (int64_t)b * sb;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int v = v0 + l + 32 * j;
-        if (v < V) {
-          const float sc = acc[i][j] + to_f(bp[v]);
-          if (better(sc, v, best, bi)) { best = sc; bi = v; }
+        for (int j = 0; j < 4; ++j) {
+          const int v = v0 + l + 32 * j;
+          if (v < V) {
+            const float sc = acc[i][j] + to_f(bp[v]);
+            if (better(sc, v, best, bi)) { best = sc; bi = v; }
+          }
         }
       }
+      warp_argmax(best, bi);
+      if (l == 0 && row < rows) atomicMax(packed + row, pack_best(best, (uint32_t)bi));
     }
-    warp_argmax(best, bi);
-    if (l == 0 && row < rows) atomicMax(packed + row, pack_best(best, (uint32_t)bi));
-  }
-  if (arrive_last(ticket + blockIdx.y, gridDim.x, &s_last)) {
-    if (tid < SR_RT) {
-      const int row = row0 + tid;
-      if (row < rows) {
-        const unsigned long long pk = atomicExch(packed + row, 0ull);
-        const int n = row / Bm1, b = row % Bm1;
-        blk[(int64_t)n * B + 1 + b] = (int64_t)packed_idx(pk);
-        if (win) win[row] = packed_val(pk);
+    if (arrive_last(ticket + blockIdx.y, gridDim.x, &s_last)) {
+      if (tid < SR_RT) {
+        const int row = row0 + tid;
+        if (row < rows) {
+          const unsigned long long pk = atomicExch(packed + row, 0ull);
+          const int n = row / Bm1, b = row % Bm1;
+          blk[(int64_t)n * B + 1 + b] = (int64_t)packed_idx(pk);
+          if (win) win[row] = packed_val(pk);
+        }
       }
+      if (tid == 0) ticket[blockIdx.y] = 0u;
     }
-    if (tid == 0) ticket[blockIdx.y] = 0u;
   }
 }
 

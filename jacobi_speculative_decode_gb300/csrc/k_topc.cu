@@ -470,7 +470,10 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const char* __restrict
 }
 
 // Per pass: one CTA per draft row.  Groups of 8 lanes score one candidate.
-template <typename T>
+// NQ > 0: r = NQ * 8 lanes * (16 / sizeof(T)) exactly; every lane issues its NQ
+// 16-byte loads of the candidate's w2 row together, the base value is loaded beside
+// them, and the next candidate's id is loaded while this one is scored.
+template <typename T, int NQ>
 __global__ void __launch_bounds__(256) topc_readout_kernel(
     const T* __restrict__ lat, const T* __restrict__ base_c, const int64_t* __restrict__ cand,
     const T* __restrict__ w2c, const T* __restrict__ w2, int Bm1, int B, int V, int C, int r,
@@ -490,13 +493,34 @@ __global__ void __launch_bounds__(256) topc_readout_kernel(
   const T* bcrow = base_c + (int64_t)row * C;
   constexpr int E = 16 / sizeof(T);
   const bool vec = (r % (8 * E)) == 0;
+  int64_t id_next = g < C ? crow[g] : 0;
   for (int k0 = 0; k0 < C; k0 += 32) {     // uniform trip count: shuffles see full warps
     const int k = k0 + g;
     const bool ok = k < C;
-    float acc = 0.f;
+    float acc = 0.f, bc = 0.f;
     int64_t id = 0;
-    if (ok) {
+    if constexpr (NQ > 0) {
+      const int64_t id_raw = id_next;
+      if (k + 32 < C) id_next = crow[k + 32];
+      if (ok) {
+        id = checked_token(id_raw, V, err);
+        bc = to_f(bcrow[k]);
+        const uint4* wr = reinterpret_cast<const uint4*>(w2c ? w2c + ((int64_t)row * C + k) * r
+                                                             : w2 + id * r);
+        uint4 u[NQ];
+#pragma unroll
+        for (int j = 0; j < NQ; ++j) u[j] = __ldg(wr + gl + 8 * j);
+#pragma unroll
+        for (int j = 0; j < NQ; ++j) {
+          const T* e = reinterpret_cast<const T*>(&u[j]);
+          const float* lq = s_lat + (gl + 8 * j) * E;
+#pragma unroll
+          for (int i = 0; i < E; ++i) acc = fmaf(to_f(e[i]), lq[i], acc);
+        }
+      }
+    } else if (ok) {
       id = checked_token(crow[k], V, err);
+      bc = to_f(bcrow[k]);
       const T* wr = w2c ? w2c + ((int64_t)row * C + k) * r : w2 + id * r;
       if (vec) {
         for (int q = gl; q < r / E; q += 8) {
@@ -513,7 +537,7 @@ __global__ void __launch_bounds__(256) topc_readout_kernel(
     acc += __shfl_xor_sync(0xFFFFFFFFu, acc, 2);
     acc += __shfl_xor_sync(0xFFFFFFFFu, acc, 4);
     if (ok) {
-      const float sc = to_f(bcrow[k]) + acc;
+      const float sc = bc + acc;
       if (better(sc, (int)id, best, bid)) { best = sc; bid = (int)id; bk = k; }
     }
   }
@@ -586,13 +610,28 @@ cudaError_t xp_launch_topc_readout(const xp_head* h, const void* lat, const void
                                    int64_t* blk, float* win, cudaStream_t s) {
   const int Bm1 = h->B - 1, rows = N * Bm1;
   const size_t smem = sizeof(float) * h->r;
-  if (h->dtype == XP_BF16)
-    topc_readout_kernel<bf16><<<rows, 256, smem, s>>>(
-        (const bf16*)lat, (const bf16*)base_c, cand, (const bf16*)w2c, (const bf16*)h->w2, Bm1,
-        h->B, h->V, C, h->r, blk, win, h->err);
-  else
-    topc_readout_kernel<float><<<rows, 256, smem, s>>>(
-        (const float*)lat, (const float*)base_c, cand, (const float*)w2c, (const float*)h->w2,
-        Bm1, h->B, h->V, C, h->r, blk, win, h->err);
+  // 16-byte loads per lane and candidate when r is a multiple of 8 lanes x 16 bytes
+  const int E = (int)(16 / xp_elem(h->dtype));
+  const int nq = h->r % (8 * E) == 0 ? h->r / (8 * E) : 0;
+#define XP_TOPC_SCORE(T, NQ)                                                                    \
+  topc_readout_kernel<T, NQ><<<rows, 256, smem, s>>>((const T*)lat, (const T*)base_c, cand,     \
+                                                     (const T*)w2c, (const T*)h->w2, Bm1, h->B, \
+                                                     h->V, C, h->r, blk, win, h->err)
+  if (h->dtype == XP_BF16) {
+    switch (nq) {
+      case 1: XP_TOPC_SCORE(bf16, 1); break;
+      case 2: XP_TOPC_SCORE(bf16, 2); break;
+      case 4: XP_TOPC_SCORE(bf16, 4); break;
+      default: XP_TOPC_SCORE(bf16, 0);
+    }
+  } else {
+    switch (nq) {
+      case 1: XP_TOPC_SCORE(float, 1); break;
+      case 2: XP_TOPC_SCORE(float, 2); break;
+      case 4: XP_TOPC_SCORE(float, 4); break;
+      default: XP_TOPC_SCORE(float, 0);
+    }
+  }
+#undef XP_TOPC_SCORE
   return cudaGetLastError();
 }
