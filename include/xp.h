@@ -224,6 +224,13 @@ xp_status xp_jacobi_refine(const xp_head* head, const void* base, int64_t stride
  * XP_OK, XP_EBADTOKEN, XP_ERANGE or XP_ETIMEOUT (precedence in reverse order). */
 xp_status xp_get_error(const xp_head* head, cudaStream_t stream);
 
+/* Failure-path self-test (no counterpart on the pages): launches one kernel whose
+ * mbarrier wait nothing will ever complete.  Like every wait in this library it
+ * gives up after about half a second and records XP_ETIMEOUT in the head's error
+ * word (read it with xp_get_error); no trap, no fault, the context stays usable.
+ * Returns XP_OK when the launch succeeded. */
+xp_status xp_selftest_wait_timeout(const xp_head* head, cudaStream_t stream);
+
 /* Name of the readout kernel the head uses for its shape (for profiling). */
 const char* xp_readout_kernel_name(const xp_head* head);
 

@@ -55,6 +55,7 @@ _SIGS = {
     "xp_readout_argmax": (_I, [_P, _P, _P, _I64, _I64, _I, _P, _P, _P, _P]),
     "xp_readout_argmax_noalloc": (_I, [_P, _P, _P, _I64, _I64, _I, _P, _P, _P]),
     "xp_refine_logits": (_I, [_P, _P, _P, _I64, _I64, _I, _P, _I64, _P]),
+    "xp_selftest_wait_timeout": (_I, [_P, _P]),
     "xp_init_argmax": (_I, [_P, _P, _I64, _I64, _P, _I, _P, _P, _P, _P]),
     "xp_topc_gather": (_I, [_P, _P, _I64, _I64, _I, _I, _P, _P, _P, _P, _P]),
     "xp_topc_readout_argmax": (_I, [_P, _P, _P, _P, _P, _I, _I, _P, _P, _P]),
@@ -180,6 +181,11 @@ def xp_readout_argmax_noalloc(head, lat, base, stride_n, stride_b, N, blk, win_v
     _check("xp_readout_argmax_noalloc", lib().xp_readout_argmax_noalloc(
         head, _ptr(lat), _ptr(base), stride_n, stride_b, N, _ptr(blk), _ptr(win_val),
         _stream(stream)))
+
+
+def xp_selftest_wait_timeout(head, stream=None):
+    """Launch one wait that can only end by its time limit (sets XP_ETIMEOUT)."""
+    _check("xp_selftest_wait_timeout", lib().xp_selftest_wait_timeout(head, _stream(stream)))
 
 
 def xp_refine_logits(head, lat, base, stride_n, stride_b, N, out, ld_out, stream=None):
