@@ -65,18 +65,20 @@ __device__ __forceinline__ float silu(float z) { return z / (1.0f + __expf(-z));
 
 // After this CTA merged its per-row candidates into `packed` with atomicMax,
 // take a ticket on `ticket`; the CTA that arrives last (ticket == expected-1)
-// returns true and must publish + reset.  No CTA waits for another.
+// returns true and must publish + reset.  No CTA waits for another.  One thread
+// takes the ticket with an acquire-release atomic after the CTA barrier: the
+// release covers every thread's earlier atomics (the barrier orders them before
+// it), and in the last CTA the acquire orders the other CTAs' atomics before the
+// publish that follows the second barrier.
 __device__ __forceinline__ bool arrive_last(unsigned* ticket, unsigned expected, int* s_flag) {
-  __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) {
-    unsigned t = atomicAdd(ticket, 1u);
+    unsigned t;
+    asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], 1;" : "=r"(t) : "l"(ticket) : "memory");
     *s_flag = (t == expected - 1u);
   }
   __syncthreads();
-  bool last = *s_flag != 0;
-  if (last) __threadfence();
-  return last;
+  return *s_flag != 0;
 }
 
 }  // namespace xpd
