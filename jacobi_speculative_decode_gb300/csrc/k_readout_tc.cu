@@ -393,6 +393,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) readout_tc_kernel(
       atomicMax(packed + grow, pack_best(best, (uint32_t)bi));
   }
 
+  ptx::tc_fence_before();
+  __syncthreads();
+  // the cluster barrier and the TMEM release come before the publish: only the publishing
+  // CTA stays on its SM for it, its cluster peers leave as soon as the cluster is done
+  if (MC > 1) {                 // peers may still multicast into this CTA or arrive on it
+    ptx::cluster_arrive_release();
+    ptx::cluster_wait();
+  }
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, TMEM_COLS);
+  }
   // ---------------- publish: the last CTA of this row tile writes blk ----------------
   ptx::pdl_wait();            // blk may still be read by the kernel this one overlapped
   const bool last = !EMIT && arrive_last(ticket + tile, (unsigned)n_seg, &bars->last);
@@ -413,16 +425,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) readout_tc_kernel(
       }
     }
     if (threadIdx.x == 0) ticket[tile] = 0u;
-  }
-  ptx::tc_fence_before();
-  __syncthreads();
-  if (MC > 1) {                 // peers may still multicast into this CTA or arrive on it
-    ptx::cluster_arrive_release();
-    ptx::cluster_wait();
-  }
-  if (warp == 1) {
-    ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem, TMEM_COLS);
   }
 }
 
