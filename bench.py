@@ -90,7 +90,8 @@ class Clocks:
     def __init__(self, index):
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
+        out_dir = os.environ.get("XP_BENCH_OUT", os.path.join(ROOT, "bench_out"))
+        self.path = os.path.join(out_dir, f"clocks_rank{index}.csv")
 
     def __enter__(self):
         try:
