@@ -6,6 +6,7 @@
 // lives in tensor memory as the MMA's A operand, so shared memory holds only the
 // two streams.  Per vocabulary tile:
 //   TMA   w2[v-tile, k-chunk]  (192 x 64 bf16, 128B-swizzled)  -> 6-stage smem ring
+//         (4 stages in the logits mode, EMIT below, which needs room for its output)
 //   TMA   base[rows, 64 ids]   (one box per 64-id third)        -> 3-stage smem ring
 //         (one tile; each thread lifts its row's part of a stage into registers as
 //         soon as the tile before it has been reduced, which frees the stage for the
@@ -13,7 +14,7 @@
 //   MMA   tcgen05 M=128 (rows) x N=192 (vocab) x K=r, A from TMEM, fp32 accumulators
 //         in TMEM, double-buffered (2 x 192 columns; A takes the last 128 columns)
 //   epilogue: each thread owns one row (one TMEM lane), adds base, keeps a
-//         running (max, lowest id) -- the logits never leave the SM.
+//         running (max, lowest id) -- in the argmax mode the logits never leave the SM.
 // Per-row winners of all CTAs of a row tile merge through a packed atomicMax;
 // the CTA that arrives last publishes into blk and resets the partials.
 //
