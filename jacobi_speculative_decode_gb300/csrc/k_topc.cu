@@ -30,6 +30,14 @@ __device__ __forceinline__ float key_value(uint32_t k, bf16*) {
 __device__ __forceinline__ float key_value(uint32_t k, float*) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
+// the stored value a radix key came from (exact; a zero key is read from `p` instead,
+// since -0 and +0 share it)
+__device__ __forceinline__ bf16 key_store(uint32_t k, bf16*) {
+  return __float2bfloat16_rn(key_value(k, (bf16*)nullptr));
+}
+__device__ __forceinline__ float key_store(uint32_t k, float*) {
+  return key_value(k, (float*)nullptr);
+}
 // bit i set when x[i] >= t (packed bf16 pair compares for bf16)
 __device__ __forceinline__ uint32_t ge_mask8(const bf16 (&x)[8], float t) {
   const __nv_bfloat162* v = reinterpret_cast<const __nv_bfloat162*>(x);
@@ -177,6 +185,7 @@ __global__ void __launch_bounds__(TS_THREADS, 2) topc_select_kernel(
   int* eqid = cid + TS_CAP;                                     // ids whose key == thr
   const int W = (V + 31) / 32;
   uint32_t* selm = reinterpret_cast<uint32_t*>(eqid + TS_CAP);  // selected ids, one bit each
+  uint16_t* wpre = reinterpret_cast<uint16_t*>(selm + W);         // selected ids below word w
   __shared__ uint32_t s_warp[32];
   __shared__ uint32_t s_sel[3];   // prefix, remaining quota, count above the prefix
   __shared__ uint32_t s_count;
@@ -253,17 +262,22 @@ __global__ void __launch_bounds__(TS_THREADS, 2) topc_select_kernel(
       if (slot < (uint32_t)TS_CAP) { ckey[slot] = k; cid[slot] = v; }
     };
     if constexpr (VEC && sizeof(T) == 2) {
-      // bf16 rows: 8 raw 16-byte words per thread in flight, packed-pair tests
-      constexpr int U = 8;
+      // bf16 rows: batches of 4 raw 16-byte words per thread, the next batch loaded
+      // before this one is tested (two batches in flight), packed-pair tests
+      constexpr int U = 4;
       const __nv_bfloat162 t2 = __float2bfloat162_rn(t0v);   // t0v is a bf16 value: exact
-      for (int c0 = tid * 8; c0 < V; c0 += U * TS_THREADS * 8) {
-        uint4 w[U];
+      uint4 w[U], wn[U];
+      auto load = [&](uint4 (&dst)[U], int c0) {
 #pragma unroll
         for (int u = 0; u < U; ++u) {
           const int v0 = c0 + u * TS_THREADS * 8;
-          w[u] = v0 + 8 <= V ? __ldg(reinterpret_cast<const uint4*>(p + v0))
-                             : make_uint4(0, 0, 0, 0);
+          dst[u] = v0 + 8 <= V ? __ldg(reinterpret_cast<const uint4*>(p + v0))
+                               : make_uint4(0, 0, 0, 0);
         }
+      };
+      load(w, tid * 8);
+      for (int c0 = tid * 8; c0 < V; c0 += U * TS_THREADS * 8) {
+        load(wn, c0 + U * TS_THREADS * 8);
 #pragma unroll
         for (int u = 0; u < U; ++u) {
           const int v0 = c0 + u * TS_THREADS * 8;
@@ -279,6 +293,8 @@ __global__ void __launch_bounds__(TS_THREADS, 2) topc_select_kernel(
             }
           }
         }
+#pragma unroll
+        for (int u = 0; u < U; ++u) w[u] = wn[u];
       }
       // the ragged end of the row (fewer than 8 elements), element by element
       for (int v = (V / 8) * 8 + tid; v < V; v += TS_THREADS)
@@ -338,18 +354,26 @@ __global__ void __launch_bounds__(TS_THREADS, 2) topc_select_kernel(
       __syncthreads();
       const int wpt = (W + TS_THREADS - 1) / TS_THREADS, w0 = tid * wpt, w1 = min(W, w0 + wpt);
       uint32_t cnt, tot;
-      // emit the selection in id order
+      // emit the selection in id order: every bitmap word's exclusive prefix count, then
+      // each selected collected entry writes itself at its rank (its value comes from
+      // its key, not from another read of the row)
       cnt = 0;
       for (int w = w0; w < w1; ++w) cnt += __popc(selm[w]);
       uint32_t pos = block_incl_scan(cnt, s_warp, &tot) - cnt;
       for (int w = w0; w < w1; ++w) {
-        uint32_t m = selm[w];
-        while (m) {
-          const int id = w * 32 + (__ffs(m) - 1);
-          crow[pos] = id;
-          brow[pos] = p[id];
-          ++pos;
-          m &= m - 1;
+        wpre[w] = (uint16_t)pos;
+        pos += __popc(selm[w]);
+      }
+      __syncthreads();
+      const uint32_t zkey = radix_key(T(0.0f));
+      for (uint32_t j = tid; j < ncol; j += TS_THREADS) {
+        const uint32_t k = ckey[j];
+        const int id = cid[j];
+        const uint32_t word = selm[id >> 5], bit = 1u << (id & 31);
+        if (word & bit) {
+          const uint32_t at = wpre[id >> 5] + __popc(word & (bit - 1u));
+          crow[at] = id;
+          brow[at] = k == zkey ? p[id] : key_store(k, (T*)nullptr);
         }
       }
     }
@@ -571,7 +595,7 @@ cudaError_t xp_launch_topc_gather(const xp_head* h, const void* base, int64_t sn
   const bool vec = (uintptr_t)base % 16 == 0 && sn % E == 0 && sb % E == 0;
   // fast path: room for the collected candidates, the boundary ids and an id bitmap
   const size_t smem_hist = (size_t)TS_HISTS * 256 * 4;
-  const size_t smem_fast = smem_hist + (size_t)TS_CAP * 12 + (size_t)((h->V + 31) / 32) * 4;
+  const size_t smem_fast = smem_hist + (size_t)TS_CAP * 12 + (size_t)((h->V + 31) / 32) * 6;
   const bool fast = C <= TS_CAP / 2 && smem_fast <= 160 * 1024;
   const size_t smem = fast ? smem_fast : smem_hist;
   cudaError_t e = cudaSuccess;
