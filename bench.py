@@ -196,8 +196,14 @@ def run_native(args, rank, world, local):
 
     passes = wl.K * args.steps * world
     value = passes / (ms / 1e3)
-    # hidden cache (3 kernels) + init (1) or top-C select and gather (2) + 2 per pass
-    launches_per_step = 3 + 1 + 2 * wl.K if wl.topc == 0 else 3 + 2 + 2 * wl.K
+    # tensor-core hidden cache (GEMM + reduce) and the init beside it (3), or the hidden
+    # cache and the top-C select (+ the w2 row copy when it is no larger than w2); then
+    # 2 per pass (latent, readout)
+    if wl.topc == 0:
+        launches_per_step = 3 + 2 * wl.K
+    else:
+        copies = 1 if wl.N * (wl.B - 1) * min(wl.topc, wl.V) <= wl.V else 0
+        launches_per_step = 2 + 1 + copies + 2 * wl.K
     out = {
         "metric": "Jacobi passes/s at N=32,B=16,V=151936 bf16; % of HBM roofline",
         "value": round(value, 2), "unit": "passes/s", "n_gpus": world, "steps": args.steps,
