@@ -82,3 +82,41 @@ def test_validation_without_device(lib):
     assert L.xp_fold_mix(1, 1, 4, 4, 9, None) == xp.XP_EINVAL
     assert L.xp_workspace_init(None, 16, None) == xp.XP_EINVAL
     assert L.xp_head_create(None, 1, 1, None, ctypes.byref(out)) == xp.XP_EINVAL
+
+
+def _header_prototypes():
+    """name -> list of parameter declarations, from include/xp.h (comments removed)."""
+    src = open(os.path.join(ROOT, "include", "xp.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    protos = {}
+    for m in re.finditer(r"\b(xp_[a-z_0-9]+)\s*\(([^;{]*?)\)\s*;", src):
+        params = [p.strip() for p in m.group(2).split(",") if p.strip() and p.strip() != "void"]
+        protos[m.group(1)] = params
+    return protos
+
+
+def _ctype_class(decl):
+    """The ctypes kind a C parameter declaration marshals to (pointer, int64, size, int)."""
+    d = " ".join(decl.split())
+    if "*" in d:
+        return "ptr"
+    if "cudaStream_t" in d:
+        return "ptr"
+    if d.startswith("int64_t") or d.startswith("const int64_t"):
+        return "i64"
+    if d.startswith("size_t"):
+        return "size"
+    return "int"
+
+
+def test_binding_signatures_match_the_header():
+    # every ctypes argument list has the header's arity and the same kind per position,
+    # so a binding cannot silently drop, add or narrow an argument
+    protos = _header_prototypes()
+    kinds = {ctypes.c_void_p: "ptr", ctypes.c_int64: "i64", ctypes.c_size_t: "size",
+             ctypes.c_int: "int"}
+    for name, (_, args) in xp._SIGS.items():
+        assert name in protos, name
+        want = [_ctype_class(d) for d in protos[name]]
+        got = [kinds.get(a, "ptr") for a in args]   # struct pointers marshal as pointers
+        assert got == want, f"{name}: binding {got} != header {want}"
