@@ -74,6 +74,9 @@ def test_validation_without_device(lib):
     assert L.xp_readout_argmax(None, 1, 1, 0, 0, 1, 1, None, 1, None) == xp.XP_ENOTPREPARED
     assert L.xp_jacobi_refine(None, 1, 0, 0, 1, 1, 1, 1, 1, 0, 1, 1, None) == xp.XP_ENOTPREPARED
     assert L.xp_get_error(None, None) == xp.XP_ENOTPREPARED
+    assert L.xp_refine_logits(None, 1, None, 0, 0, 1, 1, 4096, None) == xp.XP_ENOTPREPARED
+    assert L.xp_selftest_wait_timeout(None, None) == xp.XP_ENOTPREPARED
+    assert L.xp_readout_argmax_noalloc(None, 1, 1, 0, 0, 1, 1, None, None) == xp.XP_ENOTPREPARED
     # null pointers / bad shapes -> XP_EINVAL
     w = _w()
     out = ctypes.c_void_p()
