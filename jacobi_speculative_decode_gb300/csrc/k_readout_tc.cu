@@ -82,13 +82,7 @@ __device__ __forceinline__ float bf16hi(uint32_t u) { return __uint_as_float(u &
 // when has_base is 0) as fp32 rows of `out`; every thread stages its row's 32 values of
 // a chunk in the warp's swizzled 4 KB buffer, and the warp then stores four full
 // 128-byte row segments per instruction.
-//
-// MC > 1: the kernel runs in clusters of MC CTAs, the MC row tiles of one vocabulary
-// segment.  Every w2 k-chunk is then loaded once per cluster: CTA c loads rows
-// [c * BN/MC, (c+1) * BN/MC) of it and multicasts them into the same stage of every
-// CTA, and a stage is refilled only after all MC MMA issuers released it (their
-// commits arrive on the stage's empty barrier in every CTA of the cluster).
-template <int KCH, int MC, bool EMIT>
+template <int KCH, bool EMIT>
 __global__ void __launch_bounds__(NUM_THREADS, 1) readout_tc_kernel(
     const __nv_bfloat16* __restrict__ lat, const __grid_constant__ CUtensorMap tm_w2,
     const __grid_constant__ CUtensorMap tm_base, int rows, int Bm1, int B, int V, int rpt, int bpt,
@@ -115,7 +109,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) readout_tc_kernel(
     ptx::mbar_init(ptx::smem_u32(&bars->a_full), EPI_WARPS);   // every epilogue warp
     for (int s = 0; s < W2_STAGES; ++s) {
       ptx::mbar_init(ptx::smem_u32(&bars->w_full[s]), 1);
-      ptx::mbar_init(ptx::smem_u32(&bars->w_empty[s]), MC);   // one MMA commit per CTA
+      ptx::mbar_init(ptx::smem_u32(&bars->w_empty[s]), 1);    // the MMA issuer's commit
     }
     for (int s = 0; s < BASE_STAGES; ++s) {
       ptx::mbar_init(ptx::smem_u32(&bars->c_full[s]), 1);
@@ -135,14 +129,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) readout_tc_kernel(
   }
   ptx::tc_fence_before();
   __syncthreads();
-  if (MC > 1) {                 // no multicast into a peer before its barriers exist
-    ptx::cluster_arrive_relaxed();
-    ptx::cluster_wait();
-  }
   ptx::tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
-  const uint32_t crank = MC > 1 ? ptx::cluster_ctarank() : 0;
-  constexpr uint16_t kMask = (uint16_t)((1u << MC) - 1u);
   ptx::pdl_trigger();
 
   if (warp == 0) {
@@ -189,15 +177,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) readout_tc_kernel(
                               err);
           if (!ok) break;
           const uint32_t full = ptx::smem_u32(&bars->w_full[s]);
-          ptx::mbar_arrive_expect_tx(full, W2_STAGE_BYTES);   // from all MC slices
-          if (MC == 1) {
-            ptx::tma_load_2d(ptx::smem_u32(sW + s * W2_STAGE_BYTES), &tm_w2, full, kc * BK,
-                             vt * BN, pol_keep);
-          } else {
-            constexpr int SR = BN / MC;                        // rows of w2 per slice
-            ptx::tma_load_2d_mc(ptx::smem_u32(sW + s * W2_STAGE_BYTES + crank * SR * 128), &tm_w2,
-                                full, kc * BK, vt * BN + (int)crank * SR, kMask, pol_keep);
-          }
+          ptx::mbar_arrive_expect_tx(full, W2_STAGE_BYTES);
+          ptx::tma_load_2d(ptx::smem_u32(sW + s * W2_STAGE_BYTES), &tm_w2, full, kc * BK,
+                           vt * BN, pol_keep);
           ++issued[s];
         }
       }
@@ -228,10 +210,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) readout_tc_kernel(
           for (int kk = 0; kk < BK / 16; ++kk)   // A: 16 k = 8 columns per step
             ptx::mma_bf16_ts(d, tmem + A_COL + (uint32_t)(kc * 32 + kk * 8),
                              ptx::sw128_desc(b0 + kk * 32), IDESC, (kc | kk) != 0);
-          if (MC == 1)
-            ptx::mma_commit(ptx::smem_u32(&bars->w_empty[s]));
-          else
-            ptx::mma_commit_mc(ptx::smem_u32(&bars->w_empty[s]), kMask);
+          ptx::mma_commit(ptx::smem_u32(&bars->w_empty[s]));
         }
         if (ok) ptx::mma_commit(ptx::smem_u32(&bars->t_full[buf]));
       }
@@ -396,12 +375,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) readout_tc_kernel(
 
   ptx::tc_fence_before();
   __syncthreads();
-  // the cluster barrier and the TMEM release come before the publish: only the publishing
-  // CTA stays on its SM for it, its cluster peers leave as soon as the cluster is done
-  if (MC > 1) {                 // peers may still multicast into this CTA or arrive on it
-    ptx::cluster_arrive_release();
-    ptx::cluster_wait();
-  }
+  // the TMEM release comes before the publish, which only the last CTA of a row tile does
   if (warp == 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, TMEM_COLS);
@@ -447,79 +421,31 @@ bool encode(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* dims,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// CTAs of one launch that can be resident at once, in clusters of MC (queried once)
-template <int KCH, int MC>
-int resident_ctas(size_t smem) {
-  static int cached = -1;
-  if (cached >= 0) return cached;
-  int n = 0;
-  if (cudaFuncSetAttribute(readout_tc_kernel<KCH, MC, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)smem) == cudaSuccess) {
-    if (MC == 1) {
-      int per_sm = 0, dev = 0, sms = 0;
-      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, readout_tc_kernel<KCH, MC, false>,
-                                                        NUM_THREADS, smem) == cudaSuccess &&
-          cudaGetDevice(&dev) == cudaSuccess &&
-          cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
-        n = per_sm * sms;
-    } else {
-      cudaLaunchConfig_t cfg = {};
-      cfg.gridDim = dim3(MC);
-      cfg.blockDim = dim3(NUM_THREADS);
-      cfg.dynamicSmemBytes = smem;
-      cudaLaunchAttribute attr[1];
-      attr[0].id = cudaLaunchAttributeClusterDimension;
-      attr[0].val.clusterDim.x = MC;
-      attr[0].val.clusterDim.y = 1;
-      attr[0].val.clusterDim.z = 1;
-      cfg.attrs = attr;
-      cfg.numAttrs = 1;
-      int clusters = 0;
-      if (cudaOccupancyMaxActiveClusters(&clusters, readout_tc_kernel<KCH, MC, false>, &cfg) == cudaSuccess)
-        n = clusters * MC;
-    }
-  }
-  cudaGetLastError();   // a refused query only means: do not use this variant
-  cached = n;
-  return n;
-}
-
-template <int KCH, int MC>
-cudaError_t launch_mc(const xp_head* h, const void* lat, const CUtensorMap& tb, int N,
-                      int n_seg, int64_t* blk, float* win, unsigned long long* packed,
-                      unsigned* ticket, cudaStream_t s) {
+// Row tiles x vocabulary segments, one CTA each: the row tiles are spread over the SMs
+// and every row tile's vocabulary is split into as many segments as there are SMs per
+// row tile.
+template <int KCH>
+cudaError_t launch(const xp_head* h, const void* lat, const CUtensorMap& tb, int N,
+                   int64_t* blk, float* win, unsigned long long* packed, unsigned* ticket,
+                   cudaStream_t s) {
   const int Bm1 = h->B - 1, rows = N * Bm1;
   const int bpt = BM / Bm1, rpt = bpt * Bm1;
   const int n_rt = (N + bpt - 1) / bpt;
   const int nvt = (h->V + BN - 1) / BN;
+  const int n_seg = std::max(1, std::min(nvt, h->num_sms / n_rt));
   const size_t smem = smem_bytes<false>();
-  cudaError_t e = cudaFuncSetAttribute(readout_tc_kernel<KCH, MC, false>,
+  cudaError_t e = cudaFuncSetAttribute(readout_tc_kernel<KCH, false>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(n_rt * n_seg);
-  cfg.blockDim = dim3(NUM_THREADS);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  attr[1].id = cudaLaunchAttributeClusterDimension;
-  attr[1].val.clusterDim.x = MC;
-  attr[1].val.clusterDim.y = 1;
-  attr[1].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = MC > 1 ? 2 : 1;
-  const CUtensorMap& tw = MC == 1 ? h->tm_w2 : h->tm_w2_slice[MC == 2 ? 0 : 1];
-  e = cudaLaunchKernelEx(&cfg, readout_tc_kernel<KCH, MC, false>, (const __nv_bfloat16*)lat, tw, tb,
-                         rows, Bm1, h->B, h->V, rpt,
-                         bpt, n_rt, n_seg, nvt, blk, win,
-                         h->latent_mma ? (const float*)h->E : (const float*)nullptr, h->r * 4,
-                         packed, ticket, h->err, (float*)nullptr, (int64_t)0, 1);
+  e = xp_launch_pdl(readout_tc_kernel<KCH, false>, dim3(n_rt * n_seg), dim3(NUM_THREADS), smem, s,
+                    (const __nv_bfloat16*)lat, h->tm_w2, tb, rows, Bm1, h->B, h->V, rpt, bpt, n_rt,
+                    n_seg, nvt, blk, win,
+                    h->latent_mma ? (const float*)h->E : (const float*)nullptr, h->r * 4, packed,
+                    ticket, h->err, (float*)nullptr, (int64_t)0, 1);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-// Logits: row tiles x vocabulary segments as in the argmax launch, without clusters.
+// Logits: row tiles x vocabulary segments as in the argmax launch.
 template <int KCH>
 cudaError_t launch_logits(const xp_head* h, const void* lat, const CUtensorMap& tb, int has_base,
                           int N, float* out, int64_t ldo, cudaStream_t s) {
@@ -529,7 +455,7 @@ cudaError_t launch_logits(const xp_head* h, const void* lat, const CUtensorMap& 
   const int nvt = (h->V + BN - 1) / BN;
   const int n_seg = std::max(1, std::min(nvt, h->num_sms / n_rt));
   const size_t smem = smem_bytes<true>();
-  cudaError_t e = cudaFuncSetAttribute(readout_tc_kernel<KCH, 1, true>,
+  cudaError_t e = cudaFuncSetAttribute(readout_tc_kernel<KCH, true>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -542,38 +468,12 @@ cudaError_t launch_logits(const xp_head* h, const void* lat, const CUtensorMap& 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, readout_tc_kernel<KCH, 1, true>, (const __nv_bfloat16*)lat,
+  e = cudaLaunchKernelEx(&cfg, readout_tc_kernel<KCH, true>, (const __nv_bfloat16*)lat,
                          h->tm_w2, tb, rows, Bm1, h->B, h->V, rpt, bpt, n_rt, n_seg, nvt,
                          (int64_t*)nullptr, (float*)nullptr, (const float*)nullptr, 0,
                          (unsigned long long*)nullptr, (unsigned*)nullptr, h->err, out, ldo,
                          has_base);
   return e != cudaSuccess ? e : cudaGetLastError();
-}
-
-// Row tiles x vocabulary segments, one CTA each.  Clusters of MC row tiles share every
-// w2 chunk by multicast; MC is the largest of 4, 2 that divides the row tiles and lets
-// the launch fill at least as many SMs as 7/8 of the plain launch, else 1.
-template <int KCH>
-cudaError_t launch(const xp_head* h, const void* lat, const CUtensorMap& tb, int N,
-                   int64_t* blk, float* win, unsigned long long* packed, unsigned* ticket,
-                   cudaStream_t s) {
-  const int bpt = BM / (h->B - 1);
-  const int n_rt = (N + bpt - 1) / bpt;
-  const int nvt = (h->V + BN - 1) / BN;
-  const size_t smem = smem_bytes<false>();
-  auto segs = [&](int resident) { return std::min(nvt, resident / n_rt); };
-  const int seg1 = std::max(1, std::min(nvt, h->num_sms / n_rt));
-  if (h->readout_mc && n_rt % 4 == 0) {
-    const int sg = segs(resident_ctas<KCH, 4>(smem));
-    if (sg >= 1 && 8 * sg >= 7 * seg1)
-      return launch_mc<KCH, 4>(h, lat, tb, N, sg, blk, win, packed, ticket, s);
-  }
-  if (h->readout_mc && n_rt % 2 == 0) {
-    const int sg = segs(resident_ctas<KCH, 2>(smem));
-    if (sg >= 1 && 8 * sg >= 7 * seg1)
-      return launch_mc<KCH, 2>(h, lat, tb, N, sg, blk, win, packed, ticket, s);
-  }
-  return launch_mc<KCH, 1>(h, lat, tb, N, seg1, blk, win, packed, ticket, s);
 }
 
 }  // namespace
