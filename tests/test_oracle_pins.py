@@ -398,3 +398,99 @@ def test_zero_passes_is_init():
     blk, margins = O.jacobi_refine(base, rng.standard_normal((2, 4, 4)), anchor, np.array([0, 1]), 0, p)
     assert blk[:, 0].tolist() == [3, 11]
     assert np.array_equal(blk[:, 1:], np.argmax(base, -1)) and len(margins) == 1
+
+
+# ------------------------------------------------- top-C Jacobi and params ---
+
+def _brute_topc(base, C):
+    """The C best ids of every row by (value descending, id ascending), by sorting lists."""
+    N, Bm1, V = base.shape
+    keep = np.zeros(base.shape, bool)
+    for n in range(N):
+        for b in range(Bm1):
+            row = base[n, b].tolist()
+            for i in sorted(range(V), key=lambda i: (-row[i], i))[:C]:
+                keep[n, b, i] = True
+    return keep
+
+
+@pytest.mark.parametrize("seed,V,hid,r,H,B,N", [(40, 31, 5, 4, 6, 4, 2), (41, 23, 3, 3, 4, 5, 2),
+                                                 (42, 17, 4, 2, 3, 6, 1)])
+def test_topc_jacobi_equals_masked_sequential_greedy(seed, V, hid, r, H, B, N):
+    # qwen3_xpress page, top-C branch of jacobi_refine_greedy: scoring only a row's C
+    # best base candidates is full scoring with every other id pushed out of reach.  So
+    # after B-1 passes the top-C refinement must equal the pure-Python slot-by-slot
+    # greedy decode run on a base whose non-candidates are -1e30 (candidates chosen by
+    # sorting each row).  Catches candidates taken from the wrong row or slice of base,
+    # or chosen by the wrong order; C = V is the exact full-vocabulary case.
+    rng = np.random.default_rng(seed)
+    p = _rand_params(rng, V, hid, r, H, B, mix_scale=0.4)
+    h = rng.standard_normal((N, B, hid))
+    base = np.round(0.6 * rng.standard_normal((N, B - 1, V)) * 8) / 8     # ties included
+    anchor = rng.integers(0, V, N)
+    am1 = rng.integers(0, V, N)
+    for C in (1, 2, 5, V // 2, V):
+        masked = np.where(_brute_topc(base, C), base, -1e30)
+        want = O.sequential_greedy(masked, h, anchor, am1, p)
+        got, margins = O.jacobi_refine_topc(base, h, anchor, am1, B - 1, C, p)
+        assert np.array_equal(got, want), C
+        assert len(margins) == B
+
+
+def test_topc_jacobi_full_vocab_on_tiny_workload():
+    # C = V on the tiny-fp32 workload: the same blocks as the sequential greedy decode
+    wl = I.workload("tiny-fp32")
+    d = I.make_inputs(wl)
+    p = O.params_from_inputs(d, "f32")
+    h, base = O.decode(d["h_full"], "f32"), O.decode(d["base"], "f32")
+    seq = O.sequential_greedy(base, h, d["anchor"], d["am1"], p)
+    got, _ = O.jacobi_refine_topc(base, h, d["anchor"], d["am1"], wl.B - 1, wl.V, p)
+    assert np.array_equal(got, seq)
+
+
+@pytest.mark.parametrize("K", [0, 1, 3])
+def test_topc_jacobi_one_candidate_keeps_the_base_argmax(K):
+    # with one candidate per row every pass can only pick that row's best base id
+    rng = np.random.default_rng(43)
+    V, hid, r, H, B, N = 19, 4, 3, 5, 5, 3
+    p = _rand_params(rng, V, hid, r, H, B)
+    base = np.round(rng.standard_normal((N, B - 1, V)) * 4) / 4
+    anchor = np.array([2, 7, 11])
+    got, _ = O.jacobi_refine_topc(base, rng.standard_normal((N, B, hid)), anchor,
+                                  rng.integers(0, V, N), K, 1, p)
+    want = [[int(anchor[n])] + [max(range(V), key=lambda v: (base[n, b, v], -v))
+                                for b in range(B - 1)] for n in range(N)]
+    assert got.tolist() == want
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_params_from_inputs_maps_every_key_and_folds_once(dtype):
+    # qwen3_xpress page, XPressRefinerHead.__init__ (parameter names and shapes) and
+    # fold_from_raw_: every generated array lands in its own field, widened exactly,
+    # and the raw mixer is folded exactly once.  Each array holds one distinct value
+    # that bf16 represents exactly, so a swapped key shows up as a wrong value.
+    V, hid, r, H, B = 6, 5, 4, 3, 3
+    shapes = {"w1": (V, r), "down_h": (r, hid), "down_g": (r, hid), "in_proj": (r, 3 * r),
+              "w_gate": (H, r), "w_up": (H, r), "w_down": (r, H), "w2": (V, r)}
+    values = {"w1": 0.5, "down_h": -1.5, "down_g": 2.25, "in_proj": -0.375, "w_gate": 3.0,
+              "w_up": -0.0625, "w_down": 1.75, "w2": -2.5}
+    # bf16 bit patterns written by hand: sign | exponent | 7 fraction bits
+    bits = {0.5: 0x3F00, -1.5: 0xBFC0, 2.25: 0x4010, -0.375: 0xBEC0, 3.0: 0x4040,
+            -0.0625: 0xBD80, 1.75: 0x3FE0, -2.5: 0xC020, 0.25: 0x3E80}
+    def stored(v, shape):
+        if dtype == "bf16":
+            return np.full(shape, bits[v], np.uint16)
+        return np.full(shape, v, np.float32)
+    inp = {k: stored(values[k], s) for k, s in shapes.items()}
+    inp["raw_mix"] = stored(0.25, (r, B, B))
+    p = O.params_from_inputs(inp, dtype)
+    for k, v in values.items():
+        arr = getattr(p, k)
+        assert arr.shape == shapes[k] and arr.dtype == np.float64, k
+        assert (arr == v).all(), (k, np.unique(arr))
+    # folded once: 0.25 below the diagonal, 1.25 on it, 0 above (a second fold would
+    # give 2.25 on the diagonal; no fold would leave 0.25 above it)
+    want = np.array([[1.25, 0.0, 0.0], [0.25, 1.25, 0.0], [0.25, 0.25, 1.25]])
+    assert p.mix.shape == (r, B, B)
+    for c in range(r):
+        assert p.mix[c].tolist() == want.tolist()
