@@ -25,6 +25,11 @@
  *    xp_head_create/xp_head_refill (which synchronise nothing either, but
  *    read device properties).  Host-side validation runs before any launch;
  *    a call that returns an error has launched nothing.
+ *  - A head belongs to the device that was current when it was created.  Every
+ *    call that takes a head refuses (XP_EINVAL) while another device is current.
+ *  - Calls that take a workspace also take its size in bytes; a workspace smaller
+ *    than the call needs (xp_workspace_bytes for that N and topc) is refused with
+ *    XP_ECAPACITY before anything is launched.
  *  - Token ids are int64 at the boundary.  A token id outside [0, V) read by
  *    a kernel is clamped into range and raises XP_EBADTOKEN in the head's
  *    device error word (read with xp_get_error); kernels never trap.
@@ -85,11 +90,18 @@ typedef struct {
 
 typedef struct xp_head xp_head; /* opaque, host-side */
 
-/* Device bytes the head's prepared copies need (caller allocates them once). */
+/* Device bytes the head's prepared copies need (caller allocates them once).
+ * Beyond copies of the weights (about 2 * V * r * es for w1 and w2), a bf16 head with
+ * r = 256 and H = 512 also keeps the projected embedding table E = w1 . W_lat^T in
+ * fp32, V * r * 4 bytes (155 MB at V = 151936), so that each pass gathers one row of
+ * it per slot instead of multiplying W_lat; and the folded hidden-cache projection
+ * as two bf16 planes, 2 * 2r * hidden * 2 bytes (8 MB at hidden = 4096). */
 size_t xp_head_prep_bytes(const xp_weights* w);
 
 /* Device bytes of the per-call workspace for up to N blocks; topc > 0 adds
- * the candidate buffers of the top-C path (cand, base_c, w2c) for C = topc. */
+ * the candidate buffers of the top-C path for C = min(topc, V): cand and base_c,
+ * plus w2c only where xp_jacobi_refine copies the candidates' w2 rows (while
+ * N*(B-1)*C <= V; beyond that each pass reads them by id from w2). */
 size_t xp_workspace_bytes(const xp_weights* w, int N, int topc);
 
 /* Zero a workspace once after allocating it.  The argmax finish keeps its
@@ -118,10 +130,10 @@ xp_status xp_fold_mix(const void* raw_L, void* mix_L, int r, int B, xp_dtype dty
 /* Pass-invariant hidden half of in_proj, once per draft step:
  *   xh[n,b] = in_proj[:, :2r] . [down_h h[n,b] ; down_g mean_b' h[n,b']]
  * h_full: device [N, B, hidden] (head dtype); xh: device [N, B, r] fp32.
- * ws: workspace of xp_workspace_bytes(w, >= N, *).
+ * ws: workspace of ws_bytes >= xp_workspace_bytes(w, N, 0).
  * qwen3_xpress page, hidden_cache and the xh hoist in jacobi_refine_greedy. */
 xp_status xp_hidden_cache(const xp_head* head, const void* h_full, int N, float* xh,
-                          void* ws, cudaStream_t stream);
+                          void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /* Latent stage of one pass (all slots), written for slots 1..B-1:
  * blk: device [N, B] int64; am1: device [N] int64; xh: device [N, B, r] fp32;
@@ -140,12 +152,13 @@ xp_status xp_latent_pass(const xp_head* head, const int64_t* blk, const int64_t*
  * lat: device [N, B-1, r] head dtype.  base: device, draft row (n, b) starts
  * at base + n*stride_n + b*stride_b (elements), unit stride over v.  blk:
  * device [N, B] int64, slots 1..B-1 written.  win_val: device [N*(B-1)]
- * fp32 winning logits, or NULL.  ws: workspace (argmax partials).
+ * fp32 winning logits, or NULL.  ws: workspace of ws_bytes >=
+ * xp_workspace_bytes(w, N, 0) (argmax partials).
  * The [N*(B-1), V] logits are never written to memory.
  * xpress kernels page, fused_add_argmax_to_blk; qwen3_xpress page, refine_bias. */
 xp_status xp_readout_argmax(const xp_head* head, const void* lat, const void* base,
                             int64_t stride_n, int64_t stride_b, int N, int64_t* blk,
-                            float* win_val, void* ws, cudaStream_t stream);
+                            float* win_val, void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /* Unfused readout: the draft rows' logits (or the refiner bias alone) instead of
  * their argmax, for callers that sample or otherwise need the distribution:
@@ -181,11 +194,11 @@ xp_status xp_readout_argmax_noalloc(const xp_head* head, const void* lat, const 
                                     float* win_val, cudaStream_t stream);
 
 /* Initial block: blk[n,0] = anchor[n], blk[n,1+b] = argmax_v base[n,b,v].
- * Same base addressing as xp_readout_argmax.  anchor: device [N] int64.
+ * Same base addressing and workspace as xp_readout_argmax.  anchor: device [N] int64.
  * qwen3_xpress page, jacobi_refine_greedy (before the passes). */
 xp_status xp_init_argmax(const xp_head* head, const void* base, int64_t stride_n,
                          int64_t stride_b, const int64_t* anchor, int N, int64_t* blk,
-                         float* win_val, void* ws, cudaStream_t stream);
+                         float* win_val, void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /* Top-C candidates, once per draft step.  Per draft row: the C largest base
  * values (ties at the boundary to the lower id), stored in ascending id order:
@@ -210,7 +223,7 @@ xp_status xp_topc_readout_argmax(const xp_head* head, const void* lat, const voi
 /* Whole draft step: hidden cache, init argmax (or top-C gather when topc > 0),
  * then K passes of latent + readout-argmax.  blk: device [N, B] int64 (out;
  * slot 0 = anchor).  topc >= V scores the full vocabulary through the top-C
- * path with C = V.  ws: workspace of xp_workspace_bytes(w, >= N, topc).
+ * path with C = V.  ws: workspace of ws_bytes >= xp_workspace_bytes(w, N, topc).
  * Top-C: the candidates' w2 rows are copied once per step while N*(B-1)*C <= V
  * (the copy is no larger than w2); for larger batches every pass reads them by id
  * from w2 instead.  Both give the same blk.
@@ -218,7 +231,7 @@ xp_status xp_topc_readout_argmax(const xp_head* head, const void* lat, const voi
 xp_status xp_jacobi_refine(const xp_head* head, const void* base, int64_t stride_n,
                            int64_t stride_b, const void* h_full, const int64_t* anchor,
                            const int64_t* am1, int N, int K, int topc, int64_t* blk,
-                           void* ws, cudaStream_t stream);
+                           void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /* Synchronise `stream`, read and clear the head's device error word:
  * XP_OK, XP_EBADTOKEN, XP_ERANGE or XP_ETIMEOUT (precedence in reverse order). */

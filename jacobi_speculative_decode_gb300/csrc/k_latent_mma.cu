@@ -544,15 +544,17 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1) latent_
   }
 }
 
-// co-resident clusters per variant, queried once per shared-memory size
-int g_max_clusters[2] = {0, 0}, g_max_clusters_smem[2] = {0, 0};
+// co-resident clusters per variant and device, queried once per shared-memory size
+constexpr int kMaxDevices = 64;
+int g_max_clusters[kMaxDevices][2] = {}, g_max_clusters_smem[kMaxDevices][2] = {};
 
 size_t smem_bytes(int MT, int B) { return (size_t)make_plan(MT, B).total + 1024; }
 
 template <int MTILES>
-int max_clusters(int smem) {
-  int& cached = g_max_clusters[MTILES - 2];
-  if (cached > 0 && g_max_clusters_smem[MTILES - 2] == smem) return cached;
+int max_clusters(int device, int smem) {
+  const int d = device >= 0 && device < kMaxDevices ? device : 0;
+  int& cached = g_max_clusters[d][MTILES - 2];
+  if (cached > 0 && g_max_clusters_smem[d][MTILES - 2] == smem && d == device) return cached;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(CL);
   cfg.blockDim = dim3(THREADS);
@@ -563,7 +565,7 @@ int max_clusters(int smem) {
       cudaOccupancyMaxActiveClusters(&n, latent_mma_kernel<MTILES>, &cfg) != cudaSuccess || n <= 0)
     n = 1;
   cached = n;
-  g_max_clusters_smem[MTILES - 2] = smem;
+  g_max_clusters_smem[d][MTILES - 2] = smem;
   return n;
 }
 
@@ -577,7 +579,7 @@ cudaError_t launch(const xp_head* h, const int64_t* blk, const int64_t* am1, con
   if (e != cudaSuccess) return e;
   const int nb = MT / h->B;
   const int groups = (N + nb - 1) / nb;
-  const int clusters = std::min(groups, max_clusters<MTILES>(smem));
+  const int clusters = std::min(groups, max_clusters<MTILES>(h->device, smem));
   const Maps maps = {h->tm_wgu, h->tm_wd, h->tm_mixT};
   e = xp_launch_pdl(latent_mma_kernel<MTILES>, dim3(clusters * CL), dim3(THREADS), (size_t)smem,
                     s, maps, blk, am1, xh, (const float*)h->E, (bf16*)lat, N, h->B, h->V, h->err);
@@ -618,7 +620,7 @@ cudaError_t xp_launch_latent_mma(const xp_head* h, const int64_t* blk, const int
                                  const float* xh, int N, void* lat, cudaStream_t s) {
   // 32-row groups while they fit in one wave of co-resident clusters, else 48-row groups
   const int groups32 = (N + 32 / h->B - 1) / (32 / h->B);
-  if (groups32 <= max_clusters<2>((int)smem_bytes(32, h->B)) ||
+  if (groups32 <= max_clusters<2>(h->device, (int)smem_bytes(32, h->B)) ||
       smem_bytes(48, h->B) > 227 * 1024)
     return launch<2>(h, blk, am1, xh, N, lat, s);
   return launch<3>(h, blk, am1, xh, N, lat, s);

@@ -51,6 +51,8 @@ extern "C" xp_status xp_readout_argmax_noalloc(const xp_head* h, const void* lat
                                                cudaStream_t stream) {
   if (!h) return XP_ENOTPREPARED;
   if (!lat || !base || stride_n < 0 || stride_b < 0 || !blk || N < 0) return XP_EINVAL;
+  // the scratch address looked up below is the current device's: it must be the head's
+  if (!xp_on_head_device(h)) return XP_EINVAL;
   if (N > h->max_N) return XP_ECAPACITY;
   if ((int64_t)N * (h->B - 1) > kMaxRows) return XP_ECAPACITY;
   if (N == 0) return XP_OK;

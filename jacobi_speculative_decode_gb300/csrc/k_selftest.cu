@@ -27,6 +27,7 @@ __global__ void wait_timeout_kernel(uint32_t* err) {
 
 extern "C" xp_status xp_selftest_wait_timeout(const xp_head* h, cudaStream_t stream) {
   if (!h) return XP_ENOTPREPARED;
+  if (!xp_on_head_device(h)) return XP_EINVAL;
   wait_timeout_kernel<<<1, 32, 0, stream>>>(h->err);
   return cudaGetLastError() == cudaSuccess ? XP_OK : XP_ECUDA;
 }

@@ -92,11 +92,24 @@ bool valid_base(const xp_head* h, const void* base, int64_t sn, int64_t sb) {
   return base && sn >= 0 && sb >= 0;
 }
 
+bool on_head_device(const xp_head* h) { return xp_on_head_device(h); }
+
+// Workspace bytes a call over N blocks (C candidates, 0 = full vocabulary) needs.
+size_t ws_needed(const xp_head* h, int N, int C) {
+  return xp_layout(h->V, h->hidden, h->r, h->B, h->max_N, h->dtype, N, C).total;
+}
+
 }  // namespace
 
 // ---------------------------------------------------------------------------
+// The head's prepared memory, tensor maps and launch decisions belong to the device it
+// was created on; a call made while another device is current is refused.
+bool xp_on_head_device(const xp_head* h) {
+  int dev = -1;
+  return cudaGetDevice(&dev) == cudaSuccess && dev == h->device;
+}
+
 xp_ws_layout xp_layout(int V, int hidden, int r, int B, int max_N, xp_dtype dt, int N, int C) {
-  (void)V;
   (void)hidden;
   const size_t es = xp_elem(dt);
   const size_t rows_cap = (size_t)max_N * (B - 1);
@@ -117,7 +130,9 @@ xp_ws_layout xp_layout(int V, int hidden, int r, int B, int max_N, xp_dtype dt, 
   const size_t c = (size_t)std::max(C, 0);
   L.cand = take(rows * c * 8);
   L.base_c = take(rows * c * es);
-  L.w2c = take(rows * c * r * es);
+  // the candidates' w2 rows are copied once per step only while the copy is no larger
+  // than w2 (rows * C <= V); beyond that the passes read them by id from w2
+  L.w2c = take(rows * c <= (size_t)V ? rows * c * r * es : 0);
   L.total = o;
   return L;
 }
@@ -214,10 +229,10 @@ xp_status xp_fold_mix(const void* raw_L, void* mix_L, int r, int B, xp_dtype dty
 }
 
 xp_status xp_hidden_cache(const xp_head* h, const void* h_full, int N, float* xh, void* ws,
-                          cudaStream_t stream) {
+                          size_t ws_bytes, cudaStream_t stream) {
   if (!h) return XP_ENOTPREPARED;
-  if (!h_full || !xh || !ws || N < 0) return XP_EINVAL;
-  if (N > h->max_N) return XP_ECAPACITY;
+  if (!h_full || !xh || !ws || N < 0 || !on_head_device(h)) return XP_EINVAL;
+  if (N > h->max_N || ws_bytes < ws_needed(h, N, 0)) return XP_ECAPACITY;
   if (N == 0) return XP_OK;
   const xp_ws_layout L = xp_layout(h->V, h->hidden, h->r, h->B, h->max_N, h->dtype, N, 0);
   char* w = (char*)ws;
@@ -228,7 +243,7 @@ xp_status xp_hidden_cache(const xp_head* h, const void* h_full, int N, float* xh
 xp_status xp_latent_pass(const xp_head* h, const int64_t* blk, const int64_t* am1,
                          const float* xh, int N, void* lat, cudaStream_t stream) {
   if (!h) return XP_ENOTPREPARED;
-  if (!blk || !am1 || !xh || !lat || N < 0) return XP_EINVAL;
+  if (!blk || !am1 || !xh || !lat || N < 0 || !on_head_device(h)) return XP_EINVAL;
   if (N > h->max_N) return XP_ECAPACITY;
   if (N == 0) return XP_OK;
   // the tensor-core latent reads xh in 16-byte pieces and writes lat in channel pairs
@@ -255,10 +270,11 @@ static xp_status readout_impl(const xp_head* h, const void* lat, const void* bas
 
 xp_status xp_readout_argmax(const xp_head* h, const void* lat, const void* base, int64_t sn,
                             int64_t sb, int N, int64_t* blk, float* win, void* ws,
-                            cudaStream_t stream) {
+                            size_t ws_bytes, cudaStream_t stream) {
   if (!h) return XP_ENOTPREPARED;
-  if (!lat || !valid_base(h, base, sn, sb) || !blk || !ws || N < 0) return XP_EINVAL;
-  if (N > h->max_N) return XP_ECAPACITY;
+  if (!lat || !valid_base(h, base, sn, sb) || !blk || !ws || N < 0 || !on_head_device(h))
+    return XP_EINVAL;
+  if (N > h->max_N || ws_bytes < ws_needed(h, N, 0)) return XP_ECAPACITY;
   if (N == 0) return XP_OK;
   return readout_impl(h, lat, base, sn, sb, N, blk, win, ws, stream);
 }
@@ -266,7 +282,8 @@ xp_status xp_readout_argmax(const xp_head* h, const void* lat, const void* base,
 xp_status xp_refine_logits(const xp_head* h, const void* lat, const void* base, int64_t sn,
                            int64_t sb, int N, float* out, int64_t ld_out, cudaStream_t stream) {
   if (!h) return XP_ENOTPREPARED;
-  if (!lat || !out || (base && !valid_base(h, base, sn, sb)) || ld_out < h->V || N < 0)
+  if (!lat || !out || (base && !valid_base(h, base, sn, sb)) || ld_out < h->V || N < 0 ||
+      !on_head_device(h))
     return XP_EINVAL;
   if (N > h->max_N) return XP_ECAPACITY;
   if (N == 0) return XP_OK;
@@ -279,10 +296,11 @@ xp_status xp_refine_logits(const xp_head* h, const void* lat, const void* base, 
 
 xp_status xp_init_argmax(const xp_head* h, const void* base, int64_t sn, int64_t sb,
                          const int64_t* anchor, int N, int64_t* blk, float* win, void* ws,
-                         cudaStream_t stream) {
+                         size_t ws_bytes, cudaStream_t stream) {
   if (!h) return XP_ENOTPREPARED;
-  if (!valid_base(h, base, sn, sb) || !anchor || !blk || !ws || N < 0) return XP_EINVAL;
-  if (N > h->max_N) return XP_ECAPACITY;
+  if (!valid_base(h, base, sn, sb) || !anchor || !blk || !ws || N < 0 || !on_head_device(h))
+    return XP_EINVAL;
+  if (N > h->max_N || ws_bytes < ws_needed(h, N, 0)) return XP_ECAPACITY;
   if (N == 0) return XP_OK;
   const xp_ws_layout L = xp_layout(h->V, h->hidden, h->r, h->B, h->max_N, h->dtype, N, 0);
   char* w = (char*)ws;
@@ -295,7 +313,8 @@ xp_status xp_topc_gather(const xp_head* h, const void* base, int64_t sn, int64_t
                          int64_t* cand, void* base_c, void* w2c, int64_t* blk,
                          cudaStream_t stream) {
   if (!h) return XP_ENOTPREPARED;
-  if (!valid_base(h, base, sn, sb) || !cand || !base_c || N < 0 || C < 1 || C > h->V)
+  if (!valid_base(h, base, sn, sb) || !cand || !base_c || N < 0 || C < 1 || C > h->V ||
+      !on_head_device(h))
     return XP_EINVAL;
   if (N > h->max_N) return XP_ECAPACITY;
   if (N == 0) return XP_OK;
@@ -307,7 +326,8 @@ xp_status xp_topc_readout_argmax(const xp_head* h, const void* lat, const void* 
                                  const int64_t* cand, const void* w2c, int N, int C, int64_t* blk,
                                  float* win, cudaStream_t stream) {
   if (!h) return XP_ENOTPREPARED;
-  if (!lat || !base_c || !cand || !blk || N < 0 || C < 1 || C > h->V) return XP_EINVAL;
+  if (!lat || !base_c || !cand || !blk || N < 0 || C < 1 || C > h->V || !on_head_device(h))
+    return XP_EINVAL;
   if (N > h->max_N) return XP_ECAPACITY;
   if (N == 0) return XP_OK;
   return cuda_status(xp_launch_topc_readout(h, lat, base_c, cand, w2c, N, C, blk, win, stream));
@@ -315,14 +335,15 @@ xp_status xp_topc_readout_argmax(const xp_head* h, const void* lat, const void* 
 
 xp_status xp_jacobi_refine(const xp_head* h, const void* base, int64_t sn, int64_t sb,
                            const void* h_full, const int64_t* anchor, const int64_t* am1, int N,
-                           int K, int topc, int64_t* blk, void* ws, cudaStream_t stream) {
+                           int K, int topc, int64_t* blk, void* ws, size_t ws_bytes,
+                           cudaStream_t stream) {
   if (!h) return XP_ENOTPREPARED;
   if (!valid_base(h, base, sn, sb) || !h_full || !anchor || !am1 || !blk || !ws || N < 0 ||
-      K < 0 || topc < 0)
+      K < 0 || topc < 0 || !on_head_device(h))
     return XP_EINVAL;
-  if (N > h->max_N) return XP_ECAPACITY;
-  if (N == 0) return XP_OK;
   const int C = topc > 0 ? std::min(topc, h->V) : 0;
+  if (N > h->max_N || ws_bytes < ws_needed(h, N, C)) return XP_ECAPACITY;
+  if (N == 0) return XP_OK;
   const xp_ws_layout L = xp_layout(h->V, h->hidden, h->r, h->B, h->max_N, h->dtype, N, C);
   char* w = (char*)ws;
   float* xh = (float*)(w + L.xh);
@@ -381,6 +402,7 @@ xp_status xp_jacobi_refine(const xp_head* h, const void* base, int64_t sn, int64
 
 xp_status xp_get_error(const xp_head* h, cudaStream_t stream) {
   if (!h) return XP_ENOTPREPARED;
+  if (!on_head_device(h)) return XP_EINVAL;
   if (cudaStreamSynchronize(stream) != cudaSuccess) return XP_ECUDA;
   uint32_t word = 0;
   if (cudaMemcpy(&word, h->err, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
@@ -417,7 +439,6 @@ xp_encode_tiled_fn xp_get_encode_tiled() {
 
 static void decide_paths(xp_head* h) {
   h->readout_tc = 0;
-  h->readout_mc = 0;
   h->latent_mma = 0;
   h->hidden_tc = 0;
   int major = 0, minor = 0;
@@ -441,16 +462,6 @@ static void decide_paths(xp_head* h) {
                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS) {
       h->tm_w2 = tm;
       h->readout_tc = 1;
-      // the same map with half and quarter boxes, for the cluster-multicast readout
-      h->readout_mc = 1;
-      for (int i = 0; i < 2 && h->readout_mc; ++i) {
-        const cuuint32_t sbox[2] = {64, (cuuint32_t)(xp_readout_tc_tile() >> (i + 1))};
-        h->readout_mc =
-            xp_get_encode_tiled()(&h->tm_w2_slice[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, h->w2,
-                                  dims, strides, sbox, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-      }
     }
   }
 }

@@ -26,8 +26,6 @@ struct xp_head {
   int readout_tc;        // tcgen05 readout usable for this head's shapes
   int latent_mma;        // cluster tensor-core latent usable for this head's shapes
   CUtensorMap tm_w2;     // W2 [V, r] tiled map for the tcgen05 readout
-  CUtensorMap tm_w2_slice[2];  // the same with 1/2 and 1/4 of the tile's rows (multicast slices)
-  int readout_mc;        // cluster-multicast readout variants usable
   CUtensorMap tm_wgu, tm_wd, tm_mixT;  // [w_gate ; w_up] fp16 rows, w_down, mixer slices (TMA)
 };
 
@@ -48,6 +46,9 @@ struct xp_ws_layout {
 xp_ws_layout xp_layout(int V, int hidden, int r, int B, int max_N, xp_dtype dt, int N, int C);
 
 static inline size_t xp_elem(xp_dtype d) { return d == XP_BF16 ? 2 : 4; }
+
+// true when the current device is the one the head was created on
+bool xp_on_head_device(const xp_head* h);
 
 // ---- launchers (return cudaGetLastError() after launching) -----------------
 cudaError_t xp_launch_fold(const void* raw, void* mix, int r, int B, xp_dtype dt, cudaStream_t s);

@@ -50,16 +50,16 @@ _SIGS = {
     "xp_head_refill": (_I, [_P, ctypes.POINTER(xp_weights), _P]),
     "xp_head_destroy": (None, [_P]),
     "xp_fold_mix": (_I, [_P, _P, _I, _I, _I, _P]),
-    "xp_hidden_cache": (_I, [_P, _P, _I, _P, _P, _P]),
+    "xp_hidden_cache": (_I, [_P, _P, _I, _P, _P, _S, _P]),
     "xp_latent_pass": (_I, [_P, _P, _P, _P, _I, _P, _P]),
-    "xp_readout_argmax": (_I, [_P, _P, _P, _I64, _I64, _I, _P, _P, _P, _P]),
+    "xp_readout_argmax": (_I, [_P, _P, _P, _I64, _I64, _I, _P, _P, _P, _S, _P]),
     "xp_readout_argmax_noalloc": (_I, [_P, _P, _P, _I64, _I64, _I, _P, _P, _P]),
     "xp_refine_logits": (_I, [_P, _P, _P, _I64, _I64, _I, _P, _I64, _P]),
     "xp_selftest_wait_timeout": (_I, [_P, _P]),
-    "xp_init_argmax": (_I, [_P, _P, _I64, _I64, _P, _I, _P, _P, _P, _P]),
+    "xp_init_argmax": (_I, [_P, _P, _I64, _I64, _P, _I, _P, _P, _P, _S, _P]),
     "xp_topc_gather": (_I, [_P, _P, _I64, _I64, _I, _I, _P, _P, _P, _P, _P]),
     "xp_topc_readout_argmax": (_I, [_P, _P, _P, _P, _P, _I, _I, _P, _P, _P]),
-    "xp_jacobi_refine": (_I, [_P, _P, _I64, _I64, _P, _P, _P, _I, _I, _I, _P, _P, _P]),
+    "xp_jacobi_refine": (_I, [_P, _P, _I64, _I64, _P, _P, _P, _I, _I, _I, _P, _P, _S, _P]),
     "xp_get_error": (_I, [_P, _P]),
     "xp_readout_kernel_name": (ctypes.c_char_p, [_P]),
     "xp_status_str": (ctypes.c_char_p, [_I]),
@@ -105,6 +105,13 @@ def _stream(stream):
     if isinstance(stream, int):
         return stream
     return stream.cuda_stream
+
+
+def _nbytes(x):
+    """Size in bytes of a buffer given as a tensor (0 for None)."""
+    if x is None:
+        return 0
+    return x.numel() * x.element_size()
 
 
 def _check(name, code):
@@ -162,7 +169,7 @@ def xp_fold_mix(raw, mix, r, B, dtype, stream=None):
 
 def xp_hidden_cache(head, h_full, N, xh, ws, stream=None):
     _check("xp_hidden_cache", lib().xp_hidden_cache(head, _ptr(h_full), N, _ptr(xh), _ptr(ws),
-                                                    _stream(stream)))
+                                                    _nbytes(ws), _stream(stream)))
 
 
 def xp_latent_pass(head, blk, am1, xh, N, lat, stream=None):
@@ -173,7 +180,7 @@ def xp_latent_pass(head, blk, am1, xh, N, lat, stream=None):
 def xp_readout_argmax(head, lat, base, stride_n, stride_b, N, blk, win_val, ws, stream=None):
     _check("xp_readout_argmax", lib().xp_readout_argmax(
         head, _ptr(lat), _ptr(base), stride_n, stride_b, N, _ptr(blk), _ptr(win_val), _ptr(ws),
-        _stream(stream)))
+        _nbytes(ws), _stream(stream)))
 
 
 def xp_readout_argmax_noalloc(head, lat, base, stride_n, stride_b, N, blk, win_val, stream=None):
@@ -197,7 +204,7 @@ def xp_refine_logits(head, lat, base, stride_n, stride_b, N, out, ld_out, stream
 def xp_init_argmax(head, base, stride_n, stride_b, anchor, N, blk, win_val, ws, stream=None):
     _check("xp_init_argmax", lib().xp_init_argmax(
         head, _ptr(base), stride_n, stride_b, _ptr(anchor), N, _ptr(blk), _ptr(win_val),
-        _ptr(ws), _stream(stream)))
+        _ptr(ws), _nbytes(ws), _stream(stream)))
 
 
 def xp_topc_gather(head, base, stride_n, stride_b, N, C, cand, base_c, w2c, blk, stream=None):
@@ -216,7 +223,7 @@ def xp_jacobi_refine(head, base, stride_n, stride_b, h_full, anchor, am1, N, K, 
                      stream=None):
     _check("xp_jacobi_refine", lib().xp_jacobi_refine(
         head, _ptr(base), stride_n, stride_b, _ptr(h_full), _ptr(anchor), _ptr(am1), N, K, topc,
-        _ptr(blk), _ptr(ws), _stream(stream)))
+        _ptr(blk), _ptr(ws), _nbytes(ws), _stream(stream)))
 
 
 def xp_get_error(head, stream=None) -> int:

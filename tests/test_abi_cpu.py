@@ -62,7 +62,11 @@ def test_sizes(lib):
     ws0 = xp.xp_workspace_bytes(w, 32, 0)
     ws1 = xp.xp_workspace_bytes(w, 32, 512)
     rows = 32 * 15
-    assert ws1 - ws0 >= rows * 512 * (8 + 2 + 256 * 2)
+    # 480 rows x 512 candidates > V: cand and base_c only, the passes read w2 rows by id
+    assert rows * 512 * (8 + 2) <= ws1 - ws0 < rows * 512 * (8 + 2) + 4 * 1024
+    # one block x 16 candidates <= V: the step copies the candidates' w2 rows as well
+    ws2 = xp.xp_workspace_bytes(w, 1, 16)
+    assert ws2 - xp.xp_workspace_bytes(w, 1, 0) >= 15 * 16 * (8 + 2 + 256 * 2)
     assert xp.xp_head_prep_bytes(_w(B=1)) == 0            # B >= 2
     assert xp.xp_workspace_bytes(_w(dtype=7), 1, 0) == 0   # unknown dtype
 
@@ -71,8 +75,11 @@ def test_validation_without_device(lib):
     L = lib
     # no head -> XP_ENOTPREPARED, before any CUDA call
     assert L.xp_latent_pass(None, 1, 1, 1, 1, 1, None) == xp.XP_ENOTPREPARED
-    assert L.xp_readout_argmax(None, 1, 1, 0, 0, 1, 1, None, 1, None) == xp.XP_ENOTPREPARED
-    assert L.xp_jacobi_refine(None, 1, 0, 0, 1, 1, 1, 1, 1, 0, 1, 1, None) == xp.XP_ENOTPREPARED
+    assert L.xp_readout_argmax(None, 1, 1, 0, 0, 1, 1, None, 1, 1 << 20, None) == xp.XP_ENOTPREPARED
+    assert L.xp_jacobi_refine(None, 1, 0, 0, 1, 1, 1, 1, 1, 0, 1, 1, 1 << 20, None) == \
+        xp.XP_ENOTPREPARED
+    assert L.xp_hidden_cache(None, 1, 1, 1, 1, 1 << 20, None) == xp.XP_ENOTPREPARED
+    assert L.xp_init_argmax(None, 1, 0, 0, 1, 1, 1, None, 1, 1 << 20, None) == xp.XP_ENOTPREPARED
     assert L.xp_get_error(None, None) == xp.XP_ENOTPREPARED
     assert L.xp_refine_logits(None, 1, None, 0, 0, 1, 1, 4096, None) == xp.XP_ENOTPREPARED
     assert L.xp_selftest_wait_timeout(None, None) == xp.XP_ENOTPREPARED
