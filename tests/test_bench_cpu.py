@@ -24,3 +24,9 @@ def test_reference_arm_prints_one_contract_line():
     assert cb["kind"] == "oracle" and cb["value"] == out["value"] and cb["cores"] >= 1
     assert out["e2e"] == {"value": out["value"], "unit": "passes/s",
                           "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    # the timing fields describe what ran: measured samples, their total inside the run
+    ex = out["extrapolated"]
+    assert ex["passes_timed_per_step"] == 1 and ex["passes_per_step_in_value"] == 3
+    assert abs(out["ms_per_step"] * out["steps"] / 1e3 - ex["timed_s"]) < 0.01 + 0.01 * ex["timed_s"]
+    # the same workload identity as the native arm's line
+    assert set(out["config"]) == {"workload", "N", "B", "V", "r", "hidden", "H", "K", "topc"}
