@@ -244,6 +244,22 @@ xp_status xp_get_error(const xp_head* head, cudaStream_t stream);
  * Returns XP_OK when the launch succeeded. */
 xp_status xp_selftest_wait_timeout(const xp_head* head, cudaStream_t stream);
 
+/* Measurement aid (no counterpart on the pages): where xp_jacobi_refine runs all K passes
+ * in its persistent kernel (bf16 head, r = 256, H = 512, B <= 16, full vocabulary), it can
+ * record when each CTA reached each phase of each pass.  With buf (device) set, later
+ * refines of at most K passes write, per CTA c and pass k, twelve globaltimer stamps (ns) at
+ * buf[(c * K + k) * 12 + slot]: 0 the CTA's latent work of the pass starts (its tokens are
+ * final; 0 if it has none), 1 its latent work is done, 2 its readout starts (its row tile's
+ * latent is complete), 3 its readout's winners are merged; within its first latent group
+ * of the pass, 8 its tokens are read, 9 its first gathered rows have landed, 4 every CTA of
+ * its team has written its slice of the mixed latent u, 5 its SwiGLU activations are
+ * written, 6 its down-projection partials are written, 7 every CTA of its team has
+ * written its partials; 10 and 11 are unused.  Slots a CTA never reaches stay as they
+ * were.  *needed (nullable) receives
+ * the bytes K passes need.  buf = NULL turns the recording off.  The work done is the same
+ * either way.  XP_ECAPACITY when bytes is below *needed. */
+xp_status xp_profile_timeline(xp_head* head, void* buf, size_t bytes, int K, size_t* needed);
+
 /* Name of the readout kernel the head uses for its shape (for profiling). */
 const char* xp_readout_kernel_name(const xp_head* head);
 

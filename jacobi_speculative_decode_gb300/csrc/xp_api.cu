@@ -96,7 +96,7 @@ bool on_head_device(const xp_head* h) { return xp_on_head_device(h); }
 
 // Workspace bytes a call over N blocks (C candidates, 0 = full vocabulary) needs.
 size_t ws_needed(const xp_head* h, int N, int C) {
-  return xp_layout(h->V, h->hidden, h->r, h->B, h->max_N, h->dtype, N, C).total;
+  return xp_layout(h->V, h->hidden, h->r, h->H, h->B, h->max_N, h->dtype, N, C).total;
 }
 
 }  // namespace
@@ -109,7 +109,8 @@ bool xp_on_head_device(const xp_head* h) {
   return cudaGetDevice(&dev) == cudaSuccess && dev == h->device;
 }
 
-xp_ws_layout xp_layout(int V, int hidden, int r, int B, int max_N, xp_dtype dt, int N, int C) {
+xp_ws_layout xp_layout(int V, int hidden, int r, int H, int B, int max_N, xp_dtype dt, int N,
+                       int C) {
   (void)hidden;
   const size_t es = xp_elem(dt);
   const size_t rows_cap = (size_t)max_N * (B - 1);
@@ -120,12 +121,16 @@ xp_ws_layout xp_layout(int V, int hidden, int r, int B, int max_N, xp_dtype dt, 
   L.ro_ticket = take(rows_cap * 4);
   L.in_packed = take(rows_cap * 8);
   L.in_ticket = take(rows_cap * 4);
+  const bool persist = xp_persist_ok(r, H, B, dt);
+  L.pk1 = take(persist ? rows_cap * 8 : 0);
+  L.cnt = take(persist ? xp_persist_counter_words(max_N) * 4 : 0);
   L.zero_end = o;
   L.xh = take((size_t)max_N * B * r * 4);
   L.lat = take(rows_cap * r * es);
   L.part_rows = std::max(8192, 2 * max_N * B);
   L.part = take((size_t)L.part_rows * 2 * r * 4);
   L.hc = take((size_t)max_N * B * 2 * r * 4);
+  L.xbuf = take(persist ? xp_persist_xbuf_bytes(B, max_N) : 0);
   const size_t rows = (size_t)std::max(N, 0) * (B - 1);
   const size_t c = (size_t)std::max(C, 0);
   L.cand = take(rows * c * 8);
@@ -162,7 +167,7 @@ size_t xp_head_prep_bytes(const xp_weights* w) {
 size_t xp_workspace_bytes(const xp_weights* w, int N, int topc) {
   if (!valid_weights(w) || N < 0 || topc < 0) return 0;
   const int C = topc > 0 ? std::min(topc, w->V) : 0;
-  return xp_layout(w->V, w->hidden, w->r, w->B, w->max_N, w->dtype, N, C).total;
+  return xp_layout(w->V, w->hidden, w->r, w->H, w->B, w->max_N, w->dtype, N, C).total;
 }
 
 xp_status xp_workspace_init(void* ws, size_t ws_bytes, cudaStream_t stream) {
@@ -234,7 +239,7 @@ xp_status xp_hidden_cache(const xp_head* h, const void* h_full, int N, float* xh
   if (!h_full || !xh || !ws || N < 0 || !on_head_device(h)) return XP_EINVAL;
   if (N > h->max_N || ws_bytes < ws_needed(h, N, 0)) return XP_ECAPACITY;
   if (N == 0) return XP_OK;
-  const xp_ws_layout L = xp_layout(h->V, h->hidden, h->r, h->B, h->max_N, h->dtype, N, 0);
+  const xp_ws_layout L = xp_layout(h->V, h->hidden, h->r, h->H, h->B, h->max_N, h->dtype, N, 0);
   char* w = (char*)ws;
   return cuda_status(xp_launch_hidden(h, h_full, N, xh, (float*)(w + L.part), (float*)(w + L.hc),
                                       L.part_rows, stream));
@@ -255,7 +260,7 @@ xp_status xp_latent_pass(const xp_head* h, const int64_t* blk, const int64_t* am
 static xp_status readout_impl(const xp_head* h, const void* lat, const void* base, int64_t sn,
                               int64_t sb, int N, int64_t* blk, float* win, void* ws,
                               cudaStream_t stream) {
-  const xp_ws_layout L = xp_layout(h->V, h->hidden, h->r, h->B, h->max_N, h->dtype, N, 0);
+  const xp_ws_layout L = xp_layout(h->V, h->hidden, h->r, h->H, h->B, h->max_N, h->dtype, N, 0);
   char* w = (char*)ws;
   auto* packed = (unsigned long long*)(w + L.ro_packed);
   auto* ticket = (unsigned*)(w + L.ro_ticket);
@@ -302,7 +307,7 @@ xp_status xp_init_argmax(const xp_head* h, const void* base, int64_t sn, int64_t
     return XP_EINVAL;
   if (N > h->max_N || ws_bytes < ws_needed(h, N, 0)) return XP_ECAPACITY;
   if (N == 0) return XP_OK;
-  const xp_ws_layout L = xp_layout(h->V, h->hidden, h->r, h->B, h->max_N, h->dtype, N, 0);
+  const xp_ws_layout L = xp_layout(h->V, h->hidden, h->r, h->H, h->B, h->max_N, h->dtype, N, 0);
   char* w = (char*)ws;
   return cuda_status(xp_launch_init_argmax(h, base, sn, sb, anchor, N, blk, win,
                                            (unsigned long long*)(w + L.in_packed),
@@ -344,7 +349,7 @@ xp_status xp_jacobi_refine(const xp_head* h, const void* base, int64_t sn, int64
   const int C = topc > 0 ? std::min(topc, h->V) : 0;
   if (N > h->max_N || ws_bytes < ws_needed(h, N, C)) return XP_ECAPACITY;
   if (N == 0) return XP_OK;
-  const xp_ws_layout L = xp_layout(h->V, h->hidden, h->r, h->B, h->max_N, h->dtype, N, C);
+  const xp_ws_layout L = xp_layout(h->V, h->hidden, h->r, h->H, h->B, h->max_N, h->dtype, N, C);
   char* w = (char*)ws;
   float* xh = (float*)(w + L.xh);
   void* lat = w + L.lat;
@@ -362,6 +367,15 @@ xp_status xp_jacobi_refine(const xp_head* h, const void* base, int64_t sn, int64
     if (e == cudaSuccess) e = xp_launch_xh_reduce(h, N, xh, (float*)(w + L.part), splits, stream, true);
     if (e != cudaErrorNotSupported) {
       st = cuda_status(e);
+      // all K passes in one persistent launch where the shapes allow it
+      if (st == XP_OK && K > 0 && L.xbuf && xp_persist_call_ok(h, base, sn, sb, N)) {
+        const cudaError_t ep = xp_launch_persist(
+            h, base, sn, sb, N, K, xh, am1, blk, lat, (unsigned long long*)(w + L.ro_packed),
+            (unsigned long long*)(w + L.pk1), (void*)(w + L.xbuf), (unsigned*)(w + L.cnt),
+            stream);
+        if (ep == cudaSuccess) return XP_OK;
+        cudaGetLastError();   // not launched (e.g. not co-resident): the per-pass kernels
+      }
       for (int k = 0; k < K && st == XP_OK; ++k) {
         st = xp_latent_pass(h, blk, am1, xh, N, lat, stream);
         if (st == XP_OK) st = readout_impl(h, lat, base, sn, sb, N, blk, nullptr, ws, stream);
@@ -411,6 +425,16 @@ xp_status xp_get_error(const xp_head* h, cudaStream_t stream) {
   if (word & XP_ERR_TIMEOUT) return XP_ETIMEOUT;
   if (word & XP_ERR_RANGE) return XP_ERANGE;
   if (word & XP_ERR_BADTOKEN) return XP_EBADTOKEN;
+  return XP_OK;
+}
+
+xp_status xp_profile_timeline(xp_head* h, void* buf, size_t bytes, int K, size_t* needed) {
+  if (!h) return XP_ENOTPREPARED;
+  if (K < 0) return XP_EINVAL;
+  if (needed) *needed = xp_persist_timeline_bytes(h, K);
+  if (buf && bytes < xp_persist_timeline_bytes(h, K)) return XP_ECAPACITY;
+  h->timeline = buf;
+  h->timeline_bytes = buf ? bytes : 0;
   return XP_OK;
 }
 

@@ -27,6 +27,8 @@ struct xp_head {
   int latent_mma;        // cluster tensor-core latent usable for this head's shapes
   CUtensorMap tm_w2;     // W2 [V, r] tiled map for the tcgen05 readout
   CUtensorMap tm_wgu, tm_wd, tm_mixT;  // [w_gate ; w_up] fp16 rows, w_down, mixer slices (TMA)
+  void* timeline;        // optional per-CTA per-pass phase timestamps of the persistent refine
+  size_t timeline_bytes;
 };
 
 // device error word bits
@@ -37,13 +39,16 @@ enum : uint32_t { XP_ERR_BADTOKEN = 1u, XP_ERR_TIMEOUT = 2u, XP_ERR_RANGE = 4u }
 struct xp_ws_layout {
   size_t ro_packed, ro_ticket;        // readout argmax partials, per-row-tile tickets
   size_t in_packed, in_ticket;        // init argmax partials, per-row tickets
+  size_t pk1, cnt;                    // persistent refine: odd passes' argmax words, counters
   size_t zero_end;                    // [0, zero_end) must be zero between calls
   size_t xh, lat, part, hc;           // pass data and hidden-cache scratch
+  size_t xbuf;                        // persistent refine: latent partial-sum exchange
   int part_rows;                      // rows of fp32 split-K partials the scratch holds
   size_t cand, base_c, w2c;           // top-C tail (sized by the call's N and C)
   size_t total;
 };
-xp_ws_layout xp_layout(int V, int hidden, int r, int B, int max_N, xp_dtype dt, int N, int C);
+xp_ws_layout xp_layout(int V, int hidden, int r, int H, int B, int max_N, xp_dtype dt, int N,
+                       int C);
 
 static inline size_t xp_elem(xp_dtype d) { return d == XP_BF16 ? 2 : 4; }
 
@@ -112,6 +117,18 @@ cudaError_t xp_launch_logits_tc(const xp_head* h, const void* lat, const void* b
                                 int64_t sb, int N, float* out, int64_t ldo, cudaStream_t s);
 bool xp_logits_tc_call_ok(const xp_head* h, const void* lat, const void* base, int64_t sn,
                           int64_t sb, int N, const float* out, int64_t ldo);
+
+// All K passes in one persistent cooperative launch (bf16, r = 256, H = 512, B <= 16).
+bool xp_persist_ok(int r, int H, int B, xp_dtype dt);
+size_t xp_persist_xbuf_bytes(int B, int max_N);
+size_t xp_persist_counter_words(int max_N);
+size_t xp_persist_timeline_bytes(const xp_head* h, int K);
+bool xp_persist_call_ok(const xp_head* h, const void* base, int64_t sn, int64_t sb, int N);
+// returns cudaErrorNotSupported (nothing launched) when the call cannot take this path
+cudaError_t xp_launch_persist(const xp_head* h, const void* base, int64_t sn, int64_t sb, int N,
+                              int K, const float* xh, const int64_t* am1, int64_t* blk, void* lat,
+                              unsigned long long* packed0, unsigned long long* packed1,
+                              void* xbuf, unsigned* counters, cudaStream_t s);
 
 cudaError_t xp_launch_topc_gather(const xp_head* h, const void* base, int64_t sn, int64_t sb,
                                   int N, int C, int64_t* cand, void* base_c, void* w2c,

@@ -62,6 +62,7 @@ _SIGS = {
     "xp_jacobi_refine": (_I, [_P, _P, _I64, _I64, _P, _P, _P, _I, _I, _I, _P, _P, _S, _P]),
     "xp_get_error": (_I, [_P, _P]),
     "xp_readout_kernel_name": (ctypes.c_char_p, [_P]),
+    "xp_profile_timeline": (_I, [_P, _P, _S, _I, ctypes.POINTER(_S)]),
     "xp_status_str": (ctypes.c_char_p, [_I]),
 }
 
@@ -229,6 +230,15 @@ def xp_jacobi_refine(head, base, stride_n, stride_b, h_full, anchor, am1, N, K, 
 def xp_get_error(head, stream=None) -> int:
     """Synchronise the stream, read and clear the device error word; returns the status code."""
     return lib().xp_get_error(head, _stream(stream))
+
+
+def xp_profile_timeline(head, buf, K: int) -> int:
+    """Record the persistent refine's per-CTA phase stamps into buf (None: stop); returns
+    the bytes K passes need."""
+    needed = ctypes.c_size_t()
+    _check("xp_profile_timeline", lib().xp_profile_timeline(head, _ptr(buf), _nbytes(buf), K,
+                                                            ctypes.byref(needed)))
+    return needed.value
 
 
 def xp_readout_kernel_name(head) -> str:
