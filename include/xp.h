@@ -254,8 +254,8 @@ xp_status xp_selftest_wait_timeout(const xp_head* head, cudaStream_t stream);
  * of the pass, 8 its tokens are read, 9 its first gathered rows have landed, 4 every CTA of
  * its team has written its slice of the mixed latent u, 5 its SwiGLU activations are
  * written, 6 its down-projection partials are written, 7 every CTA of its team has
- * written its partials; 10 and 11 are unused.  Slots a CTA never reaches stay as they
- * were.  *needed (nullable) receives
+ * written its partials; in its readout, 10 its latent tile is in tensor memory, 11 its
+ * first vocabulary tile is reduced.  Slots a CTA never reaches stay as they were.  *needed (nullable) receives
  * the bytes K passes need.  buf = NULL turns the recording off.  The work done is the same
  * either way.  XP_ECAPACITY when bytes is below *needed. */
 xp_status xp_profile_timeline(xp_head* head, void* buf, size_t bytes, int K, size_t* needed);

@@ -162,7 +162,8 @@ struct Args {
 // winners merged, before its done count); inside the first latent round: 8 tokens shared,
 // 9 the first thread's x gathered, 4 all u slices of the team written (the copies are
 // issued), 5 activations written, 6 partials written, 7 all partials of the team written
-// (the copies are issued); 10 and 11 unused
+// (the copies are issued); 10 its latent tile is in TMEM, 11 its first vocabulary tile
+// is reduced
 constexpr int TL_SLOTS = 12;
 
 __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
@@ -736,6 +737,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) refine_persist_kernel(
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->a_full));
+        if (etid == 0) stamp(a, k, 10);
       }
       float best = -INFINITY;
       int bi = 0x7FFFFFFF;
@@ -802,6 +804,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) refine_persist_kernel(
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->t_empty[buf]));
+        if (etid == 0 && vt == vt0) stamp(a, k, 11);
         if (vt + 1 < vt1) lift((ti + 1) * QPT + third);
       }
       unsigned long long* pk = (k & 1) ? a.packed1 : a.packed0;
