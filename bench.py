@@ -28,8 +28,8 @@ sys.path.insert(0, ROOT)
 import numpy as np  # noqa: E402
 
 WORKLOAD = "batched-decode"
-PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "readout_tc_batched_decode.json")
-READOUT_SRC = os.path.join(ROOT, "jacobi_speculative_decode_gb300", "csrc", "k_readout_tc.cu")
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "refine_persist_batched_decode.json")
+PERSIST_SRC = os.path.join(ROOT, "jacobi_speculative_decode_gb300", "csrc", "k_persist.cu")
 
 
 def parse():
@@ -39,6 +39,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--K", type=int, default=None,
+                    help="passes per step (default: the workload's); for short profiler captures")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-breakdown", action="store_true")
@@ -108,14 +110,15 @@ def src_hash(path):
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-def committed_traffic(launch_rows):
-    """DRAM bytes per readout launch from the committed ncu summary, if the kernel is unchanged."""
+def committed_traffic(rows, K):
+    """DRAM bytes of one persistent launch of K passes, from the committed ncu summary (its
+    per-pass figure x K), if the kernel source is unchanged since the capture."""
     try:
         with open(PROFILE_TRAFFIC) as f:
             p = json.load(f)
-        if p.get("source_sha256_16") != src_hash(READOUT_SRC) or p.get("rows") != launch_rows:
+        if p.get("source_sha256_16") != src_hash(PERSIST_SRC) or p.get("rows") != rows:
             return None
-        return float(p["dram_bytes_per_launch"])
+        return float(p["dram_bytes_per_pass"]) * K
     except Exception:
         return None
 
@@ -195,6 +198,8 @@ def run_native(args, rank, world, local):
     from jacobi_speculative_decode_gb300 import shard
     wl = I.workload(args.workload)
     wl = I.workload(args.workload, seed=shard.rank_seed(wl.seed, rank))   # this rank's own batch
+    if args.K is not None:
+        wl = I.workload(args.workload, seed=wl.seed, K=args.K)
     d = I.make_inputs(wl)
     head, _ = xp.head_from_inputs(d, wl)
     base = xp.to_device(d["base"], wl.dtype)
@@ -239,8 +244,11 @@ def run_native(args, rank, world, local):
     # tensor-core hidden cache (GEMM + reduce) and the init beside it (3), or the hidden
     # cache and the top-C select (+ the w2 row copy when it is no larger than w2); then
     # 2 per pass (latent, readout)
+    persistent = persistent_path(xp, head, wl, base, sn, sb)
     if wl.topc == 0:
-        launches_per_step = 3 + 2 * wl.K
+        # hidden-cache GEMM, init argmax, reduce; then one persistent launch for all passes,
+        # or 2 launches per pass (latent, readout)
+        launches_per_step = 3 + (1 if persistent else 2 * wl.K)
     else:
         copies = 1 if wl.N * (wl.B - 1) * min(wl.topc, wl.V) <= wl.V else 0
         launches_per_step = 2 + 1 + copies + 2 * wl.K
@@ -361,6 +369,40 @@ def other_workloads(args):
     return res
 
 
+def persistent_path(xp, head, wl, base, sn, sb):
+    """Whether xp_jacobi_refine runs this workload's passes in the persistent kernel."""
+    return wl.topc == 0 and xp.xp_passes_persistent(head.handle, base, sn, sb, wl.N)
+
+
+def timeline_summary(xp, head, wl, step):
+    """Phase structure of the persistent kernel from one step with per-CTA stamps: the pass
+    period, each CTA's readout phase, and the part of a pass in which no CTA is in its
+    readout (the latent stage and its hand-offs, exposed)."""
+    import torch
+    need = xp.xp_profile_timeline(head.handle, None, wl.K)
+    buf = torch.zeros(need // 8, dtype=torch.int64, device="cuda")
+    xp.xp_profile_timeline(head.handle, buf, wl.K)
+    step()
+    torch.cuda.synchronize()
+    xp.xp_profile_timeline(head.handle, None, wl.K)
+    a = buf.cpu().numpy().reshape(-1, wl.K, 12).astype(np.float64) / 1e3   # us
+    rs, re = a[:, :, 2], a[:, :, 3]
+    used = rs[:, 0] > 0
+    rs, re = rs[used], re[used]
+    first = rs.min(axis=0)
+    period = np.diff(first)
+    gap = first[1:] - re[:, :-1].max(axis=0)
+    dur = (re - rs)[:, 1:]
+    return {"us_per_pass": round(float(np.median(period)), 2),
+            "readout_phase_us_median_cta": round(float(np.median(dur)), 2),
+            "readout_phase_us_slowest_cta": round(float(np.median(dur.max(axis=0))), 2),
+            "latent_gap_us": round(float(np.median(gap)), 2),
+            "latent_share_of_pass": round(float(np.median(gap / period)), 4),
+            "definition": "gap = first readout start of pass k+1 - last readout end of pass k "
+                          "(no CTA streams then: latent stage and its hand-offs); share = gap / "
+                          "pass period; medians over passes 1..K-1 of one step"}
+
+
 def breakdown(wl, head, base, sn, sb, h, anchor, am1, ws, stream, rank):
     import torch
     from jacobi_speculative_decode_gb300 import xp
@@ -402,6 +444,14 @@ def breakdown(wl, head, base, sn, sb, h, anchor, am1, ws, stream, rank):
     ro_ms = loop_us(readout)
     lat_ms = loop_us(latent)
     pass_ms = loop_us(one_pass)
+    persistent = persistent_path(xp, head, wl, base, sn, sb)
+    # the K passes alone (the persistent kernel when it applies), timed back to back
+    blk2 = blk.clone()
+    n_saved = n
+    n = 10
+    passes_ms = loop_us(lambda: xp.xp_jacobi_passes(head.handle, base, sn, sb, xh, am1, wl.N,
+                                                    wl.K, blk2, ws))
+    n = n_saved
     # the unfused readout: the same rows' fp32 logits written out instead of their argmax
     out = torch.empty(rows, wl.V, dtype=torch.float32, device="cuda")
     lg_ms = loop_us(lambda: xp.xp_refine_logits(head.handle, lat, base, sn, sb, wl.N, out, wl.V))
@@ -411,23 +461,45 @@ def breakdown(wl, head, base, sn, sb, h, anchor, am1, ws, stream, rank):
     ro_bytes = wl.V * wl.r * es + rows * wl.V * es + rows * wl.r * es + rows * 8
     lg_bytes = wl.V * wl.r * es + rows * wl.V * es + rows * wl.r * es + rows * wl.V * 4
     hbm, kind = peaks()
-    achieved = ro_bytes / (ro_ms / 1e3) / 1e9
-    traffic = committed_traffic(rows)
-    return {
-        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm,
-                     "unit": "GB/s", "frac": round(achieved / hbm, 4),
-                     "traffic": traffic, "kernel": xp.xp_readout_kernel_name(head.handle),
-                     "algorithmic_bytes_per_launch": ro_bytes,
-                     "peak_kind": f"{kind} (copy bandwidth, burst)"},
+    if persistent:
+        # the dominant kernel: one launch = K passes, each pass_bytes of algorithmic traffic
+        k_bytes = wl.K * pass_bytes(wl)
+        achieved = k_bytes / (passes_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(achieved / hbm, 4), "traffic": committed_traffic(rows, wl.K),
+                "kernel": "refine_persist_kernel (all K passes)",
+                "algorithmic_bytes_per_launch": k_bytes, "launch_us": round(passes_ms * 1e3, 2),
+                "peak_kind": f"{kind} (copy bandwidth, sustained loop of one launch per call)"}
+    else:
+        achieved = ro_bytes / (ro_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(achieved / hbm, 4), "traffic": None,
+                "kernel": xp.xp_readout_kernel_name(head.handle),
+                "algorithmic_bytes_per_launch": ro_bytes, "launch_us": round(ro_ms * 1e3, 2),
+                "peak_kind": f"{kind} (copy bandwidth, burst)"}
+    out = {
+        "roofline": roof,
         "kernel_us": {"readout_argmax": round(ro_ms * 1e3, 2), "latent": round(lat_ms * 1e3, 2),
-                      "pass": round(pass_ms * 1e3, 2)},
+                      "pass": round(pass_ms * 1e3, 2),
+                      "passes_K": round(passes_ms * 1e3, 2),
+                      "pass_in_passes_K": round(passes_ms * 1e3 / wl.K, 2),
+                      "note": "readout_argmax, latent and pass: the single-pass entry points "
+                              "chained back to back; passes_K: xp_jacobi_passes (K passes)"},
         # w2 + base rows + latents in, rows x V fp32 logits out
         "refine_logits": {"us": round(lg_ms * 1e3, 2), "bytes": lg_bytes,
                           "achieved_gbs": round(lg_bytes / (lg_ms / 1e3) / 1e9, 1),
                           "frac": round(lg_bytes / (lg_ms / 1e3) / 1e9 / hbm, 4)},
-        # what the latent stage adds to a pass: pass time minus the readout's own time
-        "latent_share_of_pass": round(max(pass_ms - ro_ms, 0.0) / pass_ms, 4),
+        # single-pass kernels: what the latent launch adds to a pass
+        "latent_share_of_pass_single_pass_kernels": round(max(pass_ms - ro_ms, 0.0) / pass_ms, 4),
     }
+    if persistent:
+        step = lambda: xp.xp_jacobi_refine(head.handle, base, sn, sb, h, anchor, am1, wl.N,
+                                           wl.K, 0, blk2, ws)
+        out["persistent"] = timeline_summary(xp, head, wl, step)
+        out["latent_share_of_pass"] = out["persistent"]["latent_share_of_pass"]
+    else:
+        out["latent_share_of_pass"] = out["latent_share_of_pass_single_pass_kernels"]
+    return out
 
 
 def e2e(wl, head, d, ws, args, stream, world):

@@ -233,6 +233,36 @@ xp_status xp_jacobi_refine(const xp_head* head, const void* base, int64_t stride
                            const int64_t* am1, int N, int K, int topc, int64_t* blk,
                            void* ws, size_t ws_bytes, cudaStream_t stream);
 
+/* The K passes of xp_jacobi_refine alone, for callers that prepare the pass-invariant
+ * inputs themselves: blk (device [N, B] int64) holds the initial block (slot 0 = anchor,
+ * slots 1..B-1 the initial tokens, e.g. from xp_init_argmax) and is refined in place; xh
+ * (device [N, B, r] fp32) is the hidden cache of xp_hidden_cache; am1 and the base
+ * addressing as for xp_jacobi_refine; ws of ws_bytes >= xp_workspace_bytes(w, N, 0).
+ * Full-vocabulary scoring.  Where the head is bf16 with r = 256, H = 512 and B <= 16, all K
+ * passes run in one persistent launch (one CTA per SM, every CTA resident at once);
+ * otherwise each pass is one latent and one readout launch.  Both give the same blk up to
+ * the latent's rounding (see xp_latent_pass).
+ * qwen3_xpress page, XPressRefinerHead.jacobi_refine_greedy (the loop over passes). */
+xp_status xp_jacobi_passes(const xp_head* head, const void* base, int64_t stride_n,
+                           int64_t stride_b, const float* xh, const int64_t* am1, int N, int K,
+                           int64_t* blk, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* How xp_jacobi_refine and xp_jacobi_passes run the passes (full vocabulary):
+ *  XP_PASSES_AUTO        the persistent launch where the shapes allow it and it is the
+ *                        faster choice (at least two row tiles of up to 128 draft rows, and
+ *                        at most one latent group per team of 8 CTAs per pass); else per stage
+ *  XP_PASSES_PERSISTENT  the persistent launch wherever the shapes allow it
+ *  XP_PASSES_PER_STAGE   one latent and one readout launch per pass
+ * The choice changes the launches, not the method: blocks agree up to the latent's
+ * rounding.  Default XP_PASSES_AUTO.  XP_EINVAL for another value. */
+enum { XP_PASSES_AUTO = 0, XP_PASSES_PERSISTENT = 1, XP_PASSES_PER_STAGE = 2 };
+xp_status xp_set_pass_mode(xp_head* head, int mode);
+
+/* 1 when a full-vocabulary refine of N blocks over this base addressing would run its
+ * passes in the persistent launch under the head's pass mode, else 0.  Host only. */
+int xp_passes_persistent(const xp_head* head, const void* base, int64_t stride_n,
+                         int64_t stride_b, int N);
+
 /* Synchronise `stream`, read and clear the head's device error word:
  * XP_OK, XP_EBADTOKEN, XP_ERANGE or XP_ETIMEOUT (precedence in reverse order). */
 xp_status xp_get_error(const xp_head* head, cudaStream_t stream);

@@ -910,6 +910,11 @@ bool xp_persist_ok(int r, int H, int B, xp_dtype dt) {
   return dt == XP_BF16 && r == R && H == TEAM * HS && B >= 2 && B <= BMAX;
 }
 
+bool xp_persist_preferred(const xp_head* h, int N) {
+  Geometry g;
+  return geometry(h, N, &g) && g.n_rt >= 2 && g.ngroups <= g.teams;
+}
+
 size_t xp_persist_xbuf_bytes(int B, int max_N) {
   const int nb = MT / B;
   const size_t groups = (size_t)(max_N + nb - 1) / nb;

@@ -338,6 +338,28 @@ xp_status xp_topc_readout_argmax(const xp_head* h, const void* lat, const void* 
   return cuda_status(xp_launch_topc_readout(h, lat, base_c, cand, w2c, N, C, blk, win, stream));
 }
 
+// K full-vocabulary passes on an initialised block: the persistent kernel where the shapes
+// allow it, else K x (latent, readout).
+static xp_status passes_impl(const xp_head* h, const void* base, int64_t sn, int64_t sb,
+                             const float* xh, const int64_t* am1, int N, int K, int64_t* blk,
+                             char* w, const xp_ws_layout& L, cudaStream_t stream) {
+  const bool persist = h->pass_mode == XP_PASSES_PERSISTENT ||
+                       (h->pass_mode == XP_PASSES_AUTO && xp_persist_preferred(h, N));
+  if (K > 0 && persist && L.xbuf && xp_persist_call_ok(h, base, sn, sb, N)) {
+    const cudaError_t ep = xp_launch_persist(
+        h, base, sn, sb, N, K, xh, am1, blk, w + L.lat, (unsigned long long*)(w + L.ro_packed),
+        (unsigned long long*)(w + L.pk1), (void*)(w + L.xbuf), (unsigned*)(w + L.cnt), stream);
+    if (ep == cudaSuccess) return XP_OK;
+    cudaGetLastError();   // not launched (e.g. not co-resident): the per-pass kernels
+  }
+  xp_status st = XP_OK;
+  for (int k = 0; k < K && st == XP_OK; ++k) {
+    st = xp_latent_pass(h, blk, am1, xh, N, w + L.lat, stream);
+    if (st == XP_OK) st = readout_impl(h, w + L.lat, base, sn, sb, N, blk, nullptr, w, stream);
+  }
+  return st;
+}
+
 xp_status xp_jacobi_refine(const xp_head* h, const void* base, int64_t sn, int64_t sb,
                            const void* h_full, const int64_t* anchor, const int64_t* am1, int N,
                            int K, int topc, int64_t* blk, void* ws, size_t ws_bytes,
@@ -368,18 +390,7 @@ xp_status xp_jacobi_refine(const xp_head* h, const void* base, int64_t sn, int64
     if (e != cudaErrorNotSupported) {
       st = cuda_status(e);
       // all K passes in one persistent launch where the shapes allow it
-      if (st == XP_OK && K > 0 && L.xbuf && xp_persist_call_ok(h, base, sn, sb, N)) {
-        const cudaError_t ep = xp_launch_persist(
-            h, base, sn, sb, N, K, xh, am1, blk, lat, (unsigned long long*)(w + L.ro_packed),
-            (unsigned long long*)(w + L.pk1), (void*)(w + L.xbuf), (unsigned*)(w + L.cnt),
-            stream);
-        if (ep == cudaSuccess) return XP_OK;
-        cudaGetLastError();   // not launched (e.g. not co-resident): the per-pass kernels
-      }
-      for (int k = 0; k < K && st == XP_OK; ++k) {
-        st = xp_latent_pass(h, blk, am1, xh, N, lat, stream);
-        if (st == XP_OK) st = readout_impl(h, lat, base, sn, sb, N, blk, nullptr, ws, stream);
-      }
+      if (st == XP_OK) st = passes_impl(h, base, sn, sb, xh, am1, N, K, blk, w, L, stream);
       return st;
     }
     cudaGetLastError();   // nothing was launched: take the general path below
@@ -391,10 +402,7 @@ xp_status xp_jacobi_refine(const xp_head* h, const void* base, int64_t sn, int64
     st = cuda_status(xp_launch_init_argmax(h, base, sn, sb, anchor, N, blk, nullptr,
                                            (unsigned long long*)(w + L.in_packed),
                                            (unsigned*)(w + L.in_ticket), stream));
-    for (int k = 0; k < K && st == XP_OK; ++k) {
-      st = xp_latent_pass(h, blk, am1, xh, N, lat, stream);
-      if (st == XP_OK) st = readout_impl(h, lat, base, sn, sb, N, blk, nullptr, ws, stream);
-    }
+    if (st == XP_OK) st = passes_impl(h, base, sn, sb, xh, am1, N, K, blk, w, L, stream);
     return st;
   }
   int64_t* cand = (int64_t*)(w + L.cand);
@@ -414,6 +422,19 @@ xp_status xp_jacobi_refine(const xp_head* h, const void* base, int64_t sn, int64
   return st;
 }
 
+xp_status xp_jacobi_passes(const xp_head* h, const void* base, int64_t sn, int64_t sb,
+                           const float* xh, const int64_t* am1, int N, int K, int64_t* blk,
+                           void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (!h) return XP_ENOTPREPARED;
+  if (!valid_base(h, base, sn, sb) || !xh || !am1 || !blk || !ws || N < 0 || K < 0 ||
+      !on_head_device(h))
+    return XP_EINVAL;
+  if (N > h->max_N || ws_bytes < ws_needed(h, N, 0)) return XP_ECAPACITY;
+  if (N == 0 || K == 0) return XP_OK;
+  const xp_ws_layout L = xp_layout(h->V, h->hidden, h->r, h->H, h->B, h->max_N, h->dtype, N, 0);
+  return passes_impl(h, base, sn, sb, xh, am1, N, K, blk, (char*)ws, L, stream);
+}
+
 xp_status xp_get_error(const xp_head* h, cudaStream_t stream) {
   if (!h) return XP_ENOTPREPARED;
   if (!on_head_device(h)) return XP_EINVAL;
@@ -426,6 +447,21 @@ xp_status xp_get_error(const xp_head* h, cudaStream_t stream) {
   if (word & XP_ERR_RANGE) return XP_ERANGE;
   if (word & XP_ERR_BADTOKEN) return XP_EBADTOKEN;
   return XP_OK;
+}
+
+xp_status xp_set_pass_mode(xp_head* h, int mode) {
+  if (!h) return XP_ENOTPREPARED;
+  if (mode != XP_PASSES_AUTO && mode != XP_PASSES_PERSISTENT && mode != XP_PASSES_PER_STAGE)
+    return XP_EINVAL;
+  h->pass_mode = mode;
+  return XP_OK;
+}
+
+int xp_passes_persistent(const xp_head* h, const void* base, int64_t sn, int64_t sb, int N) {
+  if (!h || N <= 0 || !valid_base(h, base, sn, sb)) return 0;
+  const bool persist = h->pass_mode == XP_PASSES_PERSISTENT ||
+                       (h->pass_mode == XP_PASSES_AUTO && xp_persist_preferred(h, N));
+  return persist && xp_persist_call_ok(h, base, sn, sb, N) ? 1 : 0;
 }
 
 xp_status xp_profile_timeline(xp_head* h, void* buf, size_t bytes, int K, size_t* needed) {

@@ -29,6 +29,7 @@ struct xp_head {
   CUtensorMap tm_wgu, tm_wd, tm_mixT;  // [w_gate ; w_up] fp16 rows, w_down, mixer slices (TMA)
   void* timeline;        // optional per-CTA per-pass phase timestamps of the persistent refine
   size_t timeline_bytes;
+  int pass_mode;         // XP_PASSES_AUTO / _PERSISTENT / _PER_STAGE
 };
 
 // device error word bits
@@ -124,6 +125,9 @@ size_t xp_persist_xbuf_bytes(int B, int max_N);
 size_t xp_persist_counter_words(int max_N);
 size_t xp_persist_timeline_bytes(const xp_head* h, int K);
 bool xp_persist_call_ok(const xp_head* h, const void* base, int64_t sn, int64_t sb, int N);
+// the automatic choice: at least two row tiles (the latent of one overlaps nothing else
+// otherwise) and one latent round per pass
+bool xp_persist_preferred(const xp_head* h, int N);
 // returns cudaErrorNotSupported (nothing launched) when the call cannot take this path
 cudaError_t xp_launch_persist(const xp_head* h, const void* base, int64_t sn, int64_t sb, int N,
                               int K, const float* xh, const int64_t* am1, int64_t* blk, void* lat,

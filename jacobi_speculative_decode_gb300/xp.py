@@ -16,6 +16,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libxp.so")
 
 XP_BF16, XP_F32 = 0, 1
+XP_PASSES_AUTO, XP_PASSES_PERSISTENT, XP_PASSES_PER_STAGE = 0, 1, 2
 STATUS = {0: "XP_OK", 1: "XP_EINVAL", 2: "XP_ECAPACITY", 3: "XP_ENOTPREPARED", 4: "XP_ECUDA",
           5: "XP_EBADTOKEN", 6: "XP_ETIMEOUT", 7: "XP_EUNSUPPORTED", 8: "XP_ERANGE"}
 XP_OK, XP_EINVAL, XP_ECAPACITY, XP_ENOTPREPARED, XP_ECUDA, XP_EBADTOKEN, XP_ETIMEOUT, \
@@ -60,6 +61,9 @@ _SIGS = {
     "xp_topc_gather": (_I, [_P, _P, _I64, _I64, _I, _I, _P, _P, _P, _P, _P]),
     "xp_topc_readout_argmax": (_I, [_P, _P, _P, _P, _P, _I, _I, _P, _P, _P]),
     "xp_jacobi_refine": (_I, [_P, _P, _I64, _I64, _P, _P, _P, _I, _I, _I, _P, _P, _S, _P]),
+    "xp_jacobi_passes": (_I, [_P, _P, _I64, _I64, _P, _P, _I, _I, _P, _P, _S, _P]),
+    "xp_set_pass_mode": (_I, [_P, _I]),
+    "xp_passes_persistent": (_I, [_P, _P, _I64, _I64, _I]),
     "xp_get_error": (_I, [_P, _P]),
     "xp_readout_kernel_name": (ctypes.c_char_p, [_P]),
     "xp_profile_timeline": (_I, [_P, _P, _S, _I, ctypes.POINTER(_S)]),
@@ -225,6 +229,21 @@ def xp_jacobi_refine(head, base, stride_n, stride_b, h_full, anchor, am1, N, K, 
     _check("xp_jacobi_refine", lib().xp_jacobi_refine(
         head, _ptr(base), stride_n, stride_b, _ptr(h_full), _ptr(anchor), _ptr(am1), N, K, topc,
         _ptr(blk), _ptr(ws), _nbytes(ws), _stream(stream)))
+
+
+def xp_jacobi_passes(head, base, stride_n, stride_b, xh, am1, N, K, blk, ws, stream=None):
+    """K passes on an initialised blk (refined in place), given the hidden cache xh."""
+    _check("xp_jacobi_passes", lib().xp_jacobi_passes(
+        head, _ptr(base), stride_n, stride_b, _ptr(xh), _ptr(am1), N, K, _ptr(blk), _ptr(ws),
+        _nbytes(ws), _stream(stream)))
+
+
+def xp_set_pass_mode(head, mode: int):
+    _check("xp_set_pass_mode", lib().xp_set_pass_mode(head, mode))
+
+
+def xp_passes_persistent(head, base, stride_n, stride_b, N) -> bool:
+    return bool(lib().xp_passes_persistent(head, _ptr(base), stride_n, stride_b, N))
 
 
 def xp_get_error(head, stream=None) -> int:

@@ -99,10 +99,15 @@ def test_max_batch_sampled():
     d = I.make_inputs(wl)
     dev = Dev(d, wl)
     p = O.params_from_inputs(d, wl.dtype)
-    got = _run_jacobi(dev, wl)
     blocks = np.array([0, 101, 255])
     want, margins = _oracle_jacobi(d, wl, p, blocks)
-    check_blocks(got[blocks], want, margins, "max-batch jacobi")
+    # the launches the workload gets by default, then the persistent launch forced (128 latent
+    # groups over its teams: several latent rounds per pass)
+    for mode in (xp.XP_PASSES_AUTO, xp.XP_PASSES_PERSISTENT):
+        xp.xp_set_pass_mode(dev.head.handle, mode)
+        got = _run_jacobi(dev, wl)
+        check_blocks(got[blocks], want, margins, f"max-batch jacobi, pass mode {mode}")
+    xp.xp_set_pass_mode(dev.head.handle, xp.XP_PASSES_AUTO)
     # hidden cache (hidden = 5120) on the sampled blocks
     xh = torch.empty(wl.N, wl.B, wl.r, dtype=torch.float32, device="cuda")
     xp.xp_hidden_cache(dev.head.handle, dev.h, wl.N, xh, dev.ws)
@@ -135,4 +140,69 @@ def test_topc_sampled():
     got = _run_jacobi(dev, wl, topc=C)
     want, margins = _oracle_jacobi(d, wl, p, blocks, topc=C)
     check_blocks(got[blocks], want, margins, "topc jacobi")
+    dev.close()
+
+
+def test_max_batch_readout_all_rows():
+    # every one of the 3840 draft rows x V logits of the max-batch readout, in the launch
+    # geometry the step uses (32 row tiles x 4 vocabulary segments), against fp64 logits
+    # computed by the oracle in row chunks
+    wl = I.workload("max-batch")
+    d = I.make_inputs(wl)
+    dev = Dev(d, wl)
+    p = O.params_from_inputs(d, wl.dtype)
+    lat_np = I.random_lat(wl, 45)
+    blk = dev.blk_in.clone()
+    win = torch.empty(wl.rows, dtype=torch.float32, device="cuda")
+    xp.xp_readout_argmax(dev.head.handle, xp.to_device(lat_np, wl.dtype), dev.base, dev.sn,
+                         dev.sb, wl.N, blk, win, dev.ws)
+    assert xp.xp_get_error(dev.head.handle) == xp.XP_OK
+    got = blk.cpu().numpy()[:, 1:].reshape(-1)
+    got_win = win.cpu().numpy()
+    lat = O.decode(lat_np, wl.dtype).reshape(wl.rows, wl.r)
+    base = d["base"].reshape(wl.rows, wl.V)
+    ids = np.empty(wl.rows, np.int64)
+    vals = np.empty(wl.rows)
+    margin = np.empty(wl.rows)
+    for r0 in range(0, wl.rows, 128):
+        s = O.readout(lat[r0:r0 + 128], p.w2, O.decode(base[r0:r0 + 128], wl.dtype))
+        ids[r0:r0 + 128], vals[r0:r0 + 128], margin[r0:r0 + 128] = O.argmax_lowest(s)
+    check_rows(got, ids, margin, "max-batch readout")
+    same = got == ids
+    check_close(got_win[same], vals[same], LAT_TOL[wl.dtype], "max-batch win")
+    dev.close()
+
+
+def _topc_by_definition(row, C):
+    """The C best ids of one row (value descending, ties at the boundary to the lower id),
+    ascending: every id above the C-th largest value, then the lowest ids equal to it."""
+    t = np.partition(row, row.size - C)[row.size - C]
+    above = np.nonzero(row > t)[0]
+    equal = np.nonzero(row == t)[0][: C - above.size]
+    return np.sort(np.concatenate([above, equal]))
+
+
+def test_topc_candidates_all_rows():
+    # the candidate selection of the top-C workload (3840 rows x V, C = 512, Zipf rows): all
+    # rows against the selection's definition, 32 whole blocks against the oracle itself
+    wl = I.workload("topc")
+    d = I.make_inputs(wl)
+    dev = Dev(d, wl)
+    C = wl.topc
+    cand = torch.empty(wl.N, wl.B - 1, C, dtype=torch.int64, device="cuda")
+    base_c = torch.empty(wl.N, wl.B - 1, C, dtype=torch.bfloat16, device="cuda")
+    xp.xp_topc_gather(dev.head.handle, dev.base, dev.sn, dev.sb, wl.N, C, cand, base_c, None,
+                      None)
+    assert xp.xp_get_error(dev.head.handle) == xp.XP_OK
+    got_cand = cand.cpu().numpy().reshape(wl.rows, C)
+    got_bc = xp.to_host_storage(base_c).reshape(wl.rows, C)
+    base_bits = d["base"].reshape(wl.rows, wl.V)
+    base = O.decode(base_bits, "bf16")
+    bad = [r for r in range(wl.rows) if not np.array_equal(got_cand[r], _topc_by_definition(base[r], C))]
+    assert not bad, f"{len(bad)} rows differ, first {bad[:5]}"
+    assert np.array_equal(got_bc, np.take_along_axis(base_bits, got_cand, axis=1))
+    blocks = np.arange(0, wl.N, wl.N // 32)[:32]
+    want_cand, want_bc = O.topc_select(O.decode(d["base"][blocks], "bf16"), C)
+    assert np.array_equal(got_cand.reshape(wl.N, wl.B - 1, C)[blocks], want_cand)
+    assert np.array_equal(O.decode(got_bc.reshape(wl.N, wl.B - 1, C)[blocks], "bf16"), want_bc)
     dev.close()
