@@ -30,6 +30,9 @@ import numpy as np  # noqa: E402
 WORKLOAD = "batched-decode"
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "refine_persist_batched_decode.json")
 PERSIST_SRC = os.path.join(ROOT, "jacobi_speculative_decode_gb300", "csrc", "k_persist.cu")
+READOUT_TRAFFIC = os.path.join(ROOT, "profiles", "readout_tc_batched_decode.json")
+PASS_MODES = {"auto": 0, "persistent": 1, "per-stage": 2}   # XP_PASSES_* of include/xp.h
+READOUT_SRC = os.path.join(ROOT, "jacobi_speculative_decode_gb300", "csrc", "k_readout_tc.cu")
 
 
 def parse():
@@ -46,6 +49,9 @@ def parse():
     ap.add_argument("--no-breakdown", action="store_true")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the single-request, top-C and max-batch side measurements")
+    ap.add_argument("--pass-mode", default="auto", choices=["auto", "persistent", "per-stage"],
+                    help="how the step runs its passes (xp_set_pass_mode); default: the library's "
+                         "automatic choice")
     return ap.parse_args()
 
 
@@ -110,15 +116,15 @@ def src_hash(path):
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-def committed_traffic(rows, K):
-    """DRAM bytes of one persistent launch of K passes, from the committed ncu summary (its
-    per-pass figure x K), if the kernel source is unchanged since the capture."""
+def committed_traffic(profile, src, rows, key, times=1):
+    """DRAM bytes (read + write) from a committed ncu summary: its per-unit figure `key` x
+    times, if the kernel source is unchanged since the capture and the rows match."""
     try:
-        with open(PROFILE_TRAFFIC) as f:
+        with open(profile) as f:
             p = json.load(f)
-        if p.get("source_sha256_16") != src_hash(PERSIST_SRC) or p.get("rows") != rows:
+        if p.get("source_sha256_16") != src_hash(src) or p.get("rows") != rows:
             return None
-        return float(p["dram_bytes_per_pass"]) * K
+        return float(p[key]) * times
     except Exception:
         return None
 
@@ -202,6 +208,7 @@ def run_native(args, rank, world, local):
         wl = I.workload(args.workload, seed=wl.seed, K=args.K)
     d = I.make_inputs(wl)
     head, _ = xp.head_from_inputs(d, wl)
+    xp.xp_set_pass_mode(head.handle, PASS_MODES[args.pass_mode])
     base = xp.to_device(d["base"], wl.dtype)
     h = xp.to_device(d["h_full"], wl.dtype)
     anchor = torch.from_numpy(d["anchor"]).cuda()
@@ -260,6 +267,7 @@ def run_native(args, rank, world, local):
         "data": "synthetic (seeded generator; random-init head weights)",
         "config": workload_config(wl),
         "parallelism": f"blocks sharded, {world} independent replica(s)",
+        "passes": "persistent launch" if persistent else "per stage (latent, readout)",
         "l2": l2_note(wl),
         "rows_per_s": round(value * wl.rows, 1),
         "roofline_step": roofline_step(wl, value),
@@ -269,7 +277,8 @@ def run_native(args, rank, world, local):
 
     # --- per-kernel breakdown: the same pass issued stage by stage, events per kernel
     if not args.no_breakdown:
-        out.update(breakdown(wl, head, base, sn, sb, h, anchor, am1, ws, stream, rank))
+        out.update(breakdown(wl, head, base, sn, sb, h, anchor, am1, ws, stream, rank,
+                             PASS_MODES[args.pass_mode]))
 
     # --- end to end through the C ABI with host buffers
     if not args.no_e2e:
@@ -403,7 +412,7 @@ def timeline_summary(xp, head, wl, step):
                           "pass period; medians over passes 1..K-1 of one step"}
 
 
-def breakdown(wl, head, base, sn, sb, h, anchor, am1, ws, stream, rank):
+def breakdown(wl, head, base, sn, sb, h, anchor, am1, ws, stream, rank, mode):
     import torch
     from jacobi_speculative_decode_gb300 import xp
     rows = wl.rows
@@ -445,12 +454,13 @@ def breakdown(wl, head, base, sn, sb, h, anchor, am1, ws, stream, rank):
     lat_ms = loop_us(latent)
     pass_ms = loop_us(one_pass)
     persistent = persistent_path(xp, head, wl, base, sn, sb)
-    # the K passes alone (the persistent kernel when it applies), timed back to back
+    # the K passes alone as the step runs them, timed back to back
     blk2 = blk.clone()
     n_saved = n
     n = 10
-    passes_ms = loop_us(lambda: xp.xp_jacobi_passes(head.handle, base, sn, sb, xh, am1, wl.N,
-                                                    wl.K, blk2, ws))
+    passes_K = lambda: xp.xp_jacobi_passes(head.handle, base, sn, sb, xh, am1, wl.N, wl.K, blk2,
+                                           ws)
+    passes_ms = loop_us(passes_K)
     n = n_saved
     # the unfused readout: the same rows' fp32 logits written out instead of their argmax
     out = torch.empty(rows, wl.V, dtype=torch.float32, device="cuda")
@@ -461,19 +471,27 @@ def breakdown(wl, head, base, sn, sb, h, anchor, am1, ws, stream, rank):
     ro_bytes = wl.V * wl.r * es + rows * wl.V * es + rows * wl.r * es + rows * 8
     lg_bytes = wl.V * wl.r * es + rows * wl.V * es + rows * wl.r * es + rows * wl.V * 4
     hbm, kind = peaks()
-    if persistent:
-        # the dominant kernel: one launch = K passes, each pass_bytes of algorithmic traffic
+
+    def persist_roofline(launch_ms):
+        # one launch = K passes, each pass_bytes of algorithmic traffic
         k_bytes = wl.K * pass_bytes(wl)
-        achieved = k_bytes / (passes_ms / 1e3) / 1e9
-        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
-                "frac": round(achieved / hbm, 4), "traffic": committed_traffic(rows, wl.K),
+        achieved = k_bytes / (launch_ms / 1e3) / 1e9
+        return {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(achieved / hbm, 4),
+                "traffic": committed_traffic(PROFILE_TRAFFIC, PERSIST_SRC, rows,
+                                             "dram_bytes_per_pass", wl.K),
                 "kernel": "refine_persist_kernel (all K passes)",
-                "algorithmic_bytes_per_launch": k_bytes, "launch_us": round(passes_ms * 1e3, 2),
+                "algorithmic_bytes_per_launch": k_bytes, "launch_us": round(launch_ms * 1e3, 2),
                 "peak_kind": f"{kind} (copy bandwidth, sustained loop of one launch per call)"}
+
+    if persistent:
+        roof = persist_roofline(passes_ms)
     else:
         achieved = ro_bytes / (ro_ms / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
-                "frac": round(achieved / hbm, 4), "traffic": None,
+                "frac": round(achieved / hbm, 4),
+                "traffic": committed_traffic(READOUT_TRAFFIC, READOUT_SRC, rows,
+                                             "dram_bytes_per_launch"),
                 "kernel": xp.xp_readout_kernel_name(head.handle),
                 "algorithmic_bytes_per_launch": ro_bytes, "launch_us": round(ro_ms * 1e3, 2),
                 "peak_kind": f"{kind} (copy bandwidth, burst)"}
@@ -492,9 +510,24 @@ def breakdown(wl, head, base, sn, sb, h, anchor, am1, ws, stream, rank):
         # single-pass kernels: what the latent launch adds to a pass
         "latent_share_of_pass_single_pass_kernels": round(max(pass_ms - ro_ms, 0.0) / pass_ms, 4),
     }
+    step = lambda: xp.xp_jacobi_refine(head.handle, base, sn, sb, h, anchor, am1, wl.N, wl.K, 0,
+                                       blk2, ws)
+    if not persistent and wl.topc == 0:
+        # the persistent kernel (all K passes in one launch) measured beside the automatic
+        # choice, with its phase structure
+        xp.xp_set_pass_mode(head.handle, xp.XP_PASSES_PERSISTENT)
+        if persistent_path(xp, head, wl, base, sn, sb):
+            n_saved = n
+            n = 10
+            p_launch_ms = loop_us(passes_K)
+            p_step_ms = loop_us(step)
+            n = n_saved
+            out["persistent_kernel"] = {
+                "passes_per_s_step": round(wl.K / (p_step_ms / 1e3), 1),
+                "roofline": persist_roofline(p_launch_ms),
+                **timeline_summary(xp, head, wl, step)}
+        xp.xp_set_pass_mode(head.handle, mode)
     if persistent:
-        step = lambda: xp.xp_jacobi_refine(head.handle, base, sn, sb, h, anchor, am1, wl.N,
-                                           wl.K, 0, blk2, ws)
         out["persistent"] = timeline_summary(xp, head, wl, step)
         out["latent_share_of_pass"] = out["persistent"]["latent_share_of_pass"]
     else:

@@ -238,25 +238,39 @@ xp_status xp_jacobi_refine(const xp_head* head, const void* base, int64_t stride
  * slots 1..B-1 the initial tokens, e.g. from xp_init_argmax) and is refined in place; xh
  * (device [N, B, r] fp32) is the hidden cache of xp_hidden_cache; am1 and the base
  * addressing as for xp_jacobi_refine; ws of ws_bytes >= xp_workspace_bytes(w, N, 0).
- * Full-vocabulary scoring.  Where the head is bf16 with r = 256, H = 512 and B <= 16, all K
- * passes run in one persistent launch (one CTA per SM, every CTA resident at once);
- * otherwise each pass is one latent and one readout launch.  Both give the same blk up to
- * the latent's rounding (see xp_latent_pass).
+ * Full-vocabulary scoring.  Each pass is one latent and one readout launch, or, under
+ * XP_PASSES_PERSISTENT with a bf16 head of r = 256, H = 512 and B <= 16, all K passes run
+ * in one persistent launch (one CTA per SM, every CTA resident at once).  Both give the
+ * same blk up to the latent's rounding (see xp_latent_pass).
  * qwen3_xpress page, XPressRefinerHead.jacobi_refine_greedy (the loop over passes). */
 xp_status xp_jacobi_passes(const xp_head* head, const void* base, int64_t stride_n,
                            int64_t stride_b, const float* xh, const int64_t* am1, int N, int K,
                            int64_t* blk, void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /* How xp_jacobi_refine and xp_jacobi_passes run the passes (full vocabulary):
- *  XP_PASSES_AUTO        the persistent launch where the shapes allow it and it is the
- *                        faster choice (at least two row tiles of up to 128 draft rows, and
- *                        at most one latent group per team of 8 CTAs per pass); else per stage
+ *  XP_PASSES_AUTO        the faster of the two for the shapes; on GB300 that has been the
+ *                        per-stage launches at every measured shape (single request,
+ *                        batched decode, max batch), so AUTO runs them
  *  XP_PASSES_PERSISTENT  the persistent launch wherever the shapes allow it
  *  XP_PASSES_PER_STAGE   one latent and one readout launch per pass
  * The choice changes the launches, not the method: blocks agree up to the latent's
  * rounding.  Default XP_PASSES_AUTO.  XP_EINVAL for another value. */
 enum { XP_PASSES_AUTO = 0, XP_PASSES_PERSISTENT = 1, XP_PASSES_PER_STAGE = 2 };
 xp_status xp_set_pass_mode(xp_head* head, int mode);
+
+/* The tensor-core argmax readout (xp_readout_argmax, the per-stage passes, the
+ * workspace-free readout) takes up to 128 draft rows per CTA.  When the row tiles come in
+ * an even number, on = 1 runs them as 2-CTA clusters whose two CTAs share every MMA and
+ * stage half of each w2 tile each; on = 0 (the default) keeps one CTA per row tile.  Both
+ * compute the same fp32 dot products over the same k order.  The readout's vocabulary
+ * loop is bound by the HBM stream of base rather than by shared-memory traffic, so pairs
+ * have not been faster on GB300; the setting is there for shapes where w2 traffic
+ * dominates.  XP_EINVAL for another value.  Host only. */
+xp_status xp_set_readout_pairs(xp_head* head, int on);
+
+/* 1 when an argmax readout of N blocks would run as 2-CTA pairs under the head's
+ * setting, else 0.  Host only. */
+int xp_readout_pairs(const xp_head* head, int N);
 
 /* 1 when a full-vocabulary refine of N blocks over this base addressing would run its
  * passes in the persistent launch under the head's pass mode, else 0.  Host only. */

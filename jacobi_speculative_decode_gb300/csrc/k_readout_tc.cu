@@ -23,6 +23,19 @@
 // group w % 4 and third (w - 3) / 4 of every tile; the epilogue warps also write
 // the latent tile into TMEM before the first MMA.
 //
+// CTA pairs (PAIR): when the row tiles come in even numbers, the two CTAs of a 2-CTA
+// cluster take two neighbouring row tiles over the same vocabulary range and share each
+// MMA (tcgen05 .cta_group::2, M = 256): the even CTA issues it, each CTA keeps its own
+// 128 rows of A and of the accumulators in its own tensor memory, and each stages only
+// half of every w2 tile (96 of the 192 ids) -- the MMA reads both halves.  Per tile a
+// CTA then moves 12 KB instead of 24 KB of w2 per k-chunk through shared memory, whose
+// bandwidth the w2 writes, the MMA's operand reads and the base traffic share.  The
+// odd CTA's MMA warp forwards the completion of its w2 stages to the even CTA's
+// barriers, and its epilogue warps arrive on the even CTA's barriers directly; these
+// per-stage and per-tile signals carry no fence (a fenced remote arrive costs a memory
+// barrier each, and the forwarding thread would serialise on them): what they report --
+// a TMA copy seen complete, tensor-memory reads waited for -- is already ordered.
+//
 // Every base stage is consumed by one fixed group of four warps (the ring size is a
 // multiple of the thirds per tile), and a group consumes its stages in order, so no
 // consumer ever waits on a stage more than one phase ahead of the phase it is in:
@@ -40,29 +53,35 @@ constexpr int BM = 128;           // rows per MMA (TMEM lanes)
 constexpr int BN = 192;           // vocabulary ids per tile (MMA N)
 constexpr int BK = 64;            // k per swizzled chunk (128 bytes of bf16)
 constexpr int QPT = BN / 64;      // 64-id thirds per tile
-constexpr int BASE_STAGES = QPT;  // one tile of base in smem (one more is lifted into
-                                  // registers); stage s always holds third s, so each
-                                  // stage has a single consumer group
 constexpr int EPI_WARPS = 4 * QPT;                  // one warp per (lane quadrant, third)
-constexpr int W2_STAGE_BYTES = BN * BK * 2;         // 24 KB
 constexpr int BASE_STAGE_BYTES = 128 * 64 * 2;      // 16 KB: one 64-wide box of <= 128 rows
 constexpr int NUM_THREADS = (3 + EPI_WARPS) * 32;   // 480
 constexpr int OUT_STAGE_BYTES = 32 * 32 * 4;        // logits: one warp's 32 rows x 32 ids
 
 // k-chunks of w2 in flight: the argmax kernel spends all of shared memory on its rings;
-// the logits kernel gives part of it to the per-warp staging of its output.
-template <bool EMIT>
+// the logits kernel gives part of it to the per-warp staging of its output.  A CTA of a
+// pair stages half a tile per k-chunk (12 KB): its w2 ring holds two tiles in 96 KB,
+// which leaves room for a base ring twice as deep (base comes from HBM every pass, w2
+// mostly from L2).
+template <bool EMIT, bool PAIR>
 struct Smem {
-  static constexpr int W2_STAGES = EMIT ? 4 : 6;
+  static_assert(!(EMIT && PAIR), "the logits kernel runs unpaired");
+  static constexpr int W2_ROWS = PAIR ? BN / 2 : BN;      // w2 rows this CTA stages per tile
+  static constexpr int W2_STAGE_BYTES = W2_ROWS * BK * 2;
+  static constexpr int W2_STAGES = EMIT ? 4 : (PAIR ? 8 : 6);
+  // base: one tile in smem (a pair: two), one more lifted into registers; stage s always
+  // holds third s % QPT, so each stage has a single consumer group
+  static constexpr int BASE_STAGES = PAIR ? 2 * QPT : QPT;
   static constexpr int OUT_BYTES = EMIT ? EPI_WARPS * OUT_STAGE_BYTES : 0;
+  static_assert(BASE_STAGES % QPT == 0, "a base stage always holds the same third");
 };
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t A_COL = 2 * BN;                  // latent tile: columns [384, 384 + r/2)
 constexpr uint32_t IDESC = ptx::idesc_bf16_f32(BM, BN);
+constexpr uint32_t IDESC_PAIR = ptx::idesc_bf16_f32(2 * BM, BN);   // M = 256 over the pair
 static_assert(A_COL + 128 <= TMEM_COLS, "accumulators and the latent tile share TMEM");
-static_assert(BASE_STAGES % QPT == 0, "a base stage always holds the same third");
 
-template <int W2_STAGES>
+template <int W2_STAGES, int BASE_STAGES>
 struct Bars {
   uint64_t a_full;
   uint64_t w_full[W2_STAGES], w_empty[W2_STAGES];
@@ -82,7 +101,7 @@ __device__ __forceinline__ float bf16hi(uint32_t u) { return __uint_as_float(u &
 // when has_base is 0) as fp32 rows of `out`; every thread stages its row's 32 values of
 // a chunk in the warp's swizzled 4 KB buffer, and the warp then stores four full
 // 128-byte row segments per instruction.
-template <int KCH, bool EMIT>
+template <int KCH, bool EMIT, bool PAIR>
 __global__ void __launch_bounds__(NUM_THREADS, 1) readout_tc_kernel(
     const __nv_bfloat16* __restrict__ lat, const __grid_constant__ CUtensorMap tm_w2,
     const __grid_constant__ CUtensorMap tm_base, int rows, int Bm1, int B, int V, int rpt, int bpt,
@@ -90,25 +109,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) readout_tc_kernel(
     const float* __restrict__ pf_rows, int pf_row_bytes,
     unsigned long long* __restrict__ packed, unsigned* __restrict__ ticket, uint32_t* err,
     float* __restrict__ out, int64_t ldo, int has_base) {
-  constexpr int W2_STAGES = Smem<EMIT>::W2_STAGES;
+  constexpr int W2_STAGES = Smem<EMIT, PAIR>::W2_STAGES;
+  constexpr int W2_STAGE_BYTES = Smem<EMIT, PAIR>::W2_STAGE_BYTES;
+  constexpr int BASE_STAGES = Smem<EMIT, PAIR>::BASE_STAGES;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = ptx::smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
-  uint8_t* sW = smem;                                    // W2_STAGES x 24 KB
+  uint8_t* sW = smem;                                    // W2_STAGES x 24 (pair: 12) KB
   uint8_t* sC = sW + W2_STAGES * W2_STAGE_BYTES;         // BASE_STAGES x 16 KB
   uint8_t* sO = sC + BASE_STAGES * BASE_STAGE_BYTES;    // EMIT: EPI_WARPS x 4 KB
-  auto* bars = reinterpret_cast<Bars<W2_STAGES>*>(sO + Smem<EMIT>::OUT_BYTES);
+  auto* bars = reinterpret_cast<Bars<W2_STAGES, BASE_STAGES>*>(sO + Smem<EMIT, PAIR>::OUT_BYTES);
   volatile int* abort = &bars->abort;
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int tile = blockIdx.x % n_rt, seg = blockIdx.x / n_rt;
   const int vt0 = (int)((int64_t)seg * nvt / n_seg), vt1 = (int)((int64_t)(seg + 1) * nvt / n_seg);
   const int row0 = tile * rpt;
+  // pair: rank 0 (even row tile) issues the MMAs; its a_full and t_empty also count the
+  // odd CTA's epilogue warps, its w_full the odd CTA's forwarded w2 stage
+  const uint32_t rank = PAIR ? ptx::cluster_ctarank() : 0u;
+  const uint32_t pair_n = PAIR ? 2u : 1u;
 
   if (threadIdx.x == 0) {
-    ptx::mbar_init(ptx::smem_u32(&bars->a_full), EPI_WARPS);   // every epilogue warp
+    ptx::mbar_init(ptx::smem_u32(&bars->a_full), pair_n * EPI_WARPS);   // every epilogue warp
     for (int s = 0; s < W2_STAGES; ++s) {
-      ptx::mbar_init(ptx::smem_u32(&bars->w_full[s]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bars->w_full[s]), rank == 0 ? pair_n : 1u);
       ptx::mbar_init(ptx::smem_u32(&bars->w_empty[s]), 1);    // the MMA issuer's commit
     }
     for (int s = 0; s < BASE_STAGES; ++s) {
@@ -117,18 +142,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) readout_tc_kernel(
     }
     for (int s = 0; s < 2; ++s) {
       ptx::mbar_init(ptx::smem_u32(&bars->t_full[s]), 1);
-      ptx::mbar_init(ptx::smem_u32(&bars->t_empty[s]), EPI_WARPS);
+      ptx::mbar_init(ptx::smem_u32(&bars->t_empty[s]), pair_n * EPI_WARPS);
     }
     ptx::mbar_init(ptx::smem_u32(&bars->mma_done), 1);
     bars->abort = 0;
     ptx::fence_barrier_init();
   }
   if (warp == 1) {
-    ptx::tmem_alloc(ptx::smem_u32(&bars->tmem_base), TMEM_COLS);
-    ptx::tmem_relinquish();
+    if constexpr (PAIR) {
+      ptx::tmem_alloc_pair(ptx::smem_u32(&bars->tmem_base), TMEM_COLS);
+      ptx::tmem_relinquish_pair();
+    } else {
+      ptx::tmem_alloc(ptx::smem_u32(&bars->tmem_base), TMEM_COLS);
+      ptx::tmem_relinquish();
+    }
   }
   ptx::tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR) {            // both CTAs' barriers exist before either signals the other
+    __syncwarp();
+    ptx::cluster_arrive_release();
+    ptx::cluster_wait();
+  } else {
+    __syncthreads();
+  }
   ptx::tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
   ptx::pdl_trigger();
@@ -179,7 +215,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) readout_tc_kernel(
           const uint32_t full = ptx::smem_u32(&bars->w_full[s]);
           ptx::mbar_arrive_expect_tx(full, W2_STAGE_BYTES);
           ptx::tma_load_2d(ptx::smem_u32(sW + s * W2_STAGE_BYTES), &tm_w2, full, kc * BK,
-                           vt * BN, pol_keep);
+                           vt * BN + (int)rank * Smem<EMIT, PAIR>::W2_ROWS, pol_keep);
           ++issued[s];
         }
       }
@@ -189,33 +225,65 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) readout_tc_kernel(
           ptx::mbar_wait(ptx::smem_u32(&bars->w_full[s]), (issued[s] - 1) & 1, &no_abort, err);
     }
   } else if (warp == 1) {
-    // ---------------- MMA issuer ----------------
-    if (lane == 0) {
-      bool ok = ptx::mbar_wait(ptx::smem_u32(&bars->a_full), 0, abort, err);
+    // ---------------- MMA issuer (pair: the even CTA; the odd one forwards) ----------------
+    if (lane == 0 && rank == 0) {
+      auto wait_in = [&](uint64_t* b, uint32_t parity) {
+        return ptx::mbar_wait(ptx::smem_u32(b), parity, abort, err);
+      };
+      // a commit arrives on this CTA's barrier and, in a pair, on the odd CTA's
+      auto commit = [&](uint64_t* b) {
+        if constexpr (PAIR) {
+          ptx::mma_commit_pair(ptx::smem_u32(b));
+          ptx::mma_commit_pair(ptx::peer_addr(ptx::smem_u32(b), 1));
+        } else {
+          ptx::mma_commit(ptx::smem_u32(b));
+        }
+      };
+      // a_full: the odd CTA's A rows come with a cluster-scope release
+      bool ok = PAIR ? ptx::mbar_wait_acq_cluster(ptx::smem_u32(&bars->a_full), 0, abort, err)
+                     : ptx::mbar_wait(ptx::smem_u32(&bars->a_full), 0, abort, err);
       ptx::tc_fence_after();
       int wi = 0, ti = 0;
       for (int vt = vt0; vt < vt1 && ok; ++vt, ++ti) {
         const int buf = ti & 1;
-        ok = ptx::mbar_wait(ptx::smem_u32(&bars->t_empty[buf]), ((ti >> 1) & 1) ^ 1, abort, err);
+        ok = wait_in(&bars->t_empty[buf], ((ti >> 1) & 1) ^ 1);
         if (!ok) break;
         ptx::tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(buf * BN);
         for (int kc = 0; kc < KCH && ok; ++kc, ++wi) {
           const int s = wi % W2_STAGES;
-          ok = ptx::mbar_wait(ptx::smem_u32(&bars->w_full[s]), (wi / W2_STAGES) & 1, abort, err);
+          ok = wait_in(&bars->w_full[s], (wi / W2_STAGES) & 1);
           if (!ok) break;
           ptx::tc_fence_after();
           const uint32_t b0 = ptx::smem_u32(sW + s * W2_STAGE_BYTES);
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk)   // A: 16 k = 8 columns per step
-            ptx::mma_bf16_ts(d, tmem + A_COL + (uint32_t)(kc * 32 + kk * 8),
-                             ptx::sw128_desc(b0 + kk * 32), IDESC, (kc | kk) != 0);
-          ptx::mma_commit(ptx::smem_u32(&bars->w_empty[s]));
+          for (int kk = 0; kk < BK / 16; ++kk) {  // A: 16 k = 8 columns per step
+            const uint32_t a = tmem + A_COL + (uint32_t)(kc * 32 + kk * 8);
+            if constexpr (PAIR)
+              ptx::mma_bf16_ts_pair(d, a, ptx::sw128_desc(b0 + kk * 32), IDESC_PAIR, (kc | kk) != 0);
+            else
+              ptx::mma_bf16_ts(d, a, ptx::sw128_desc(b0 + kk * 32), IDESC, (kc | kk) != 0);
+          }
+          commit(&bars->w_empty[s]);
         }
-        if (ok) ptx::mma_commit(ptx::smem_u32(&bars->t_full[buf]));
+        if (ok) commit(&bars->t_full[buf]);
       }
       // every MMA this thread issued has finished before TMEM can be released
-      ptx::mma_commit(ptx::smem_u32(&bars->mma_done));
+      commit(&bars->mma_done);
+      volatile int no_abort = 0;
+      ptx::mbar_wait(ptx::smem_u32(&bars->mma_done), 0, &no_abort, err);
+    } else if (PAIR && lane == 0) {
+      // odd CTA: tell the even CTA, in the order its MMAs consume them, that this CTA's
+      // half of each w2 stage has landed
+      int wi = 0;
+      bool ok = true;
+      for (int vt = vt0; vt < vt1 && ok; ++vt)
+        for (int kc = 0; kc < KCH && ok; ++kc, ++wi) {
+          const int s = wi % W2_STAGES;
+          ok = ptx::mbar_wait(ptx::smem_u32(&bars->w_full[s]), (wi / W2_STAGES) & 1, abort, err);
+          if (ok) ptx::mbar_arrive_remote_relaxed(ptx::peer_addr(ptx::smem_u32(&bars->w_full[s]), 0));
+        }
+      // the even CTA's last commit: no MMA reads this CTA's shared or tensor memory after it
       volatile int no_abort = 0;
       ptx::mbar_wait(ptx::smem_u32(&bars->mma_done), 0, &no_abort, err);
     }
@@ -225,6 +293,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) readout_tc_kernel(
     const int third = (warp - 3) >> 2;       // which 64 ids of every tile
     const int i = g * 32 + lane;             // row within the tile
     const uint32_t trow = tmem + ((uint32_t)(g * 32) << 16);
+    // arrive on a barrier the MMA issuer waits on: in a pair, the even CTA's (a fence-free
+    // arrive where it only reports tensor-memory reads that tcgen05.wait::ld has completed)
+    auto arrive_issuer = [&](uint64_t* b, bool release) {
+      if (PAIR && rank != 0) {
+        const uint32_t rb = ptx::peer_addr(ptx::smem_u32(b), 0);
+        if (release)
+          ptx::mbar_arrive_remote(rb);
+        else
+          ptx::mbar_arrive_remote_relaxed(rb);
+      } else {
+        ptx::mbar_arrive(ptx::smem_u32(b));
+      }
+    };
     {
       // the latent tile into TMEM columns [A_COL, A_COL + r/2): k-chunk c (64 values =
       // 32 columns) of the group's 32 rows is written by the warp with third == c % 3
@@ -258,7 +339,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) readout_tc_kernel(
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->a_full));
+      if (lane == 0) arrive_issuer(&bars->a_full, true);
     }
     float best = -INFINITY;
     int bi = 0x7FFFFFFF;
@@ -365,7 +446,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) readout_tc_kernel(
       }
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->t_empty[buf]));
+      if (lane == 0) arrive_issuer(&bars->t_empty[buf], false);
       if (vt + 1 < vt1 && has_base) ok = lift((ti + 1) * QPT + third);
     }
     const int grow = row0 + i;
@@ -374,11 +455,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) readout_tc_kernel(
   }
 
   ptx::tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR) {            // no remote arrive or MMA read of this CTA is in flight
+    __syncwarp();
+    ptx::cluster_arrive_release();
+    ptx::cluster_wait();
+  } else {
+    __syncthreads();
+  }
   // the TMEM release comes before the publish, which only the last CTA of a row tile does
   if (warp == 1) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem, TMEM_COLS);
+    if constexpr (PAIR)
+      ptx::tmem_dealloc_pair(tmem, TMEM_COLS);
+    else
+      ptx::tmem_dealloc(tmem, TMEM_COLS);
   }
   // ---------------- publish: the last CTA of this row tile writes blk ----------------
   ptx::pdl_wait();            // blk may still be read by the kernel this one overlapped
@@ -403,13 +493,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) readout_tc_kernel(
   }
 }
 
-template <bool EMIT>
+template <bool EMIT, bool PAIR>
 constexpr size_t smem_bytes() {
-  return 1024 + (size_t)Smem<EMIT>::W2_STAGES * W2_STAGE_BYTES + BASE_STAGES * BASE_STAGE_BYTES +
-         Smem<EMIT>::OUT_BYTES + sizeof(Bars<Smem<EMIT>::W2_STAGES>);
+  using S = Smem<EMIT, PAIR>;
+  return 1024 + (size_t)S::W2_STAGES * S::W2_STAGE_BYTES + S::BASE_STAGES * BASE_STAGE_BYTES +
+         S::OUT_BYTES + sizeof(Bars<S::W2_STAGES, S::BASE_STAGES>);
 }
-static_assert(smem_bytes<false>() <= 227 * 1024, "readout shared memory");
-static_assert(smem_bytes<true>() <= 227 * 1024, "logits shared memory");
+static_assert(smem_bytes<false, false>() <= 227 * 1024, "readout shared memory");
+static_assert(smem_bytes<false, true>() <= 227 * 1024, "paired readout shared memory");
+static_assert(smem_bytes<true, false>() <= 227 * 1024, "logits shared memory");
+static_assert(Smem<false, true>::W2_STAGE_BYTES % 1024 == 0, "128-byte swizzle atoms stay aligned");
 
 bool encode(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* dims,
             const cuuint64_t* strides, const cuuint32_t* box) {
@@ -423,26 +516,51 @@ bool encode(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* dims,
 
 // Row tiles x vocabulary segments, one CTA each: the row tiles are spread over the SMs
 // and every row tile's vocabulary is split into as many segments as there are SMs per
-// row tile.
-template <int KCH>
-cudaError_t launch(const xp_head* h, const void* lat, const CUtensorMap& tb, int N,
-                   int64_t* blk, float* win, unsigned long long* packed, unsigned* ticket,
-                   cudaStream_t s) {
+// row tile.  With an even number of row tiles, neighbouring row tiles of one segment
+// form a 2-CTA cluster that shares its MMAs (block x = segment * n_rt + row tile, so the
+// cluster of blocks 2c, 2c + 1 holds row tiles 2p, 2p + 1 of one segment).
+template <int KCH, bool PAIR>
+cudaError_t launch_argmax(const xp_head* h, const void* lat, const CUtensorMap& tb, int N,
+                          int64_t* blk, float* win, unsigned long long* packed,
+                          unsigned* ticket, cudaStream_t s) {
   const int Bm1 = h->B - 1, rows = N * Bm1;
   const int bpt = BM / Bm1, rpt = bpt * Bm1;
   const int n_rt = (N + bpt - 1) / bpt;
   const int nvt = (h->V + BN - 1) / BN;
   const int n_seg = std::max(1, std::min(nvt, h->num_sms / n_rt));
-  const size_t smem = smem_bytes<false>();
-  cudaError_t e = cudaFuncSetAttribute(readout_tc_kernel<KCH, false>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const size_t smem = smem_bytes<false, PAIR>();
+  auto* kern = readout_tc_kernel<KCH, false, PAIR>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  e = xp_launch_pdl(readout_tc_kernel<KCH, false>, dim3(n_rt * n_seg), dim3(NUM_THREADS), smem, s,
-                    (const __nv_bfloat16*)lat, h->tm_w2, tb, rows, Bm1, h->B, h->V, rpt, bpt, n_rt,
-                    n_seg, nvt, blk, win,
-                    h->latent_mma ? (const float*)h->E : (const float*)nullptr, h->r * 4, packed,
-                    ticket, h->err, (float*)nullptr, (int64_t)0, 1);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(n_rt * n_seg);
+  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 2;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = PAIR ? 2 : 1;
+  e = cudaLaunchKernelEx(&cfg, kern, (const __nv_bfloat16*)lat, PAIR ? h->tm_w2_half : h->tm_w2,
+                         tb, rows, Bm1, h->B, h->V, rpt, bpt, n_rt, n_seg, nvt, blk, win,
+                         h->latent_mma ? (const float*)h->E : (const float*)nullptr, h->r * 4,
+                         packed, ticket, h->err, (float*)nullptr, (int64_t)0, 1);
   return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+template <int KCH>
+cudaError_t launch(const xp_head* h, const void* lat, const CUtensorMap& tb, int N,
+                   int64_t* blk, float* win, unsigned long long* packed, unsigned* ticket,
+                   cudaStream_t s) {
+  if (xp_readout_paired(h, N))
+    return launch_argmax<KCH, true>(h, lat, tb, N, blk, win, packed, ticket, s);
+  return launch_argmax<KCH, false>(h, lat, tb, N, blk, win, packed, ticket, s);
 }
 
 // Logits: row tiles x vocabulary segments as in the argmax launch.
@@ -454,8 +572,8 @@ cudaError_t launch_logits(const xp_head* h, const void* lat, const CUtensorMap& 
   const int n_rt = (N + bpt - 1) / bpt;
   const int nvt = (h->V + BN - 1) / BN;
   const int n_seg = std::max(1, std::min(nvt, h->num_sms / n_rt));
-  const size_t smem = smem_bytes<true>();
-  cudaError_t e = cudaFuncSetAttribute(readout_tc_kernel<KCH, true>,
+  const size_t smem = smem_bytes<true, false>();
+  cudaError_t e = cudaFuncSetAttribute(readout_tc_kernel<KCH, true, false>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -468,7 +586,7 @@ cudaError_t launch_logits(const xp_head* h, const void* lat, const CUtensorMap& 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, readout_tc_kernel<KCH, true>, (const __nv_bfloat16*)lat,
+  e = cudaLaunchKernelEx(&cfg, readout_tc_kernel<KCH, true, false>, (const __nv_bfloat16*)lat,
                          h->tm_w2, tb, rows, Bm1, h->B, h->V, rpt, bpt, n_rt, n_seg, nvt,
                          (int64_t*)nullptr, (float*)nullptr, (const float*)nullptr, 0,
                          (unsigned long long*)nullptr, (unsigned*)nullptr, h->err, out, ldo,
@@ -479,6 +597,12 @@ cudaError_t launch_logits(const xp_head* h, const void* lat, const CUtensorMap& 
 }  // namespace
 
 int xp_readout_tc_tile() { return BN; }
+
+bool xp_readout_paired(const xp_head* h, int N) {
+  const int bpt = BM / (h->B - 1);
+  const int n_rt = (N + bpt - 1) / bpt;
+  return h->readout_pair_ok && h->readout_pairs && N > 0 && n_rt % 2 == 0;
+}
 
 bool xp_readout_tc_call_ok(const xp_head* h, const void* lat, const void* base, int64_t sn,
                            int64_t sb, int N) {

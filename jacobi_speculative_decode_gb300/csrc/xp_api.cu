@@ -189,6 +189,7 @@ xp_status xp_head_create(const xp_weights* w, void* prep_dev, size_t prep_bytes,
   if (!h) return XP_ECAPACITY;
   h->V = w->V; h->hidden = w->hidden; h->r = w->r; h->H = w->H; h->B = w->B;
   h->max_N = w->max_N; h->dtype = w->dtype;
+  h->readout_pairs = 0;
   h->prep = (char*)prep_dev;
   h->prep_bytes = prep_bytes;
   if (cudaGetDevice(&h->device) != cudaSuccess ||
@@ -338,8 +339,8 @@ xp_status xp_topc_readout_argmax(const xp_head* h, const void* lat, const void* 
   return cuda_status(xp_launch_topc_readout(h, lat, base_c, cand, w2c, N, C, blk, win, stream));
 }
 
-// K full-vocabulary passes on an initialised block: the persistent kernel where the shapes
-// allow it, else K x (latent, readout).
+// K full-vocabulary passes on an initialised block: K x (latent, readout), or the persistent
+// kernel when the head's pass mode asks for it and the shapes allow it.
 static xp_status passes_impl(const xp_head* h, const void* base, int64_t sn, int64_t sb,
                              const float* xh, const int64_t* am1, int N, int K, int64_t* blk,
                              char* w, const xp_ws_layout& L, cudaStream_t stream) {
@@ -457,6 +458,17 @@ xp_status xp_set_pass_mode(xp_head* h, int mode) {
   return XP_OK;
 }
 
+xp_status xp_set_readout_pairs(xp_head* h, int on) {
+  if (!h) return XP_ENOTPREPARED;
+  if (on != 0 && on != 1) return XP_EINVAL;
+  h->readout_pairs = on;
+  return XP_OK;
+}
+
+int xp_readout_pairs(const xp_head* h, int N) {
+  return h && h->readout_tc && N > 0 && N <= h->max_N && xp_readout_paired(h, N) ? 1 : 0;
+}
+
 int xp_passes_persistent(const xp_head* h, const void* base, int64_t sn, int64_t sb, int N) {
   if (!h || N <= 0 || !valid_base(h, base, sn, sb)) return 0;
   const bool persist = h->pass_mode == XP_PASSES_PERSISTENT ||
@@ -499,6 +511,7 @@ xp_encode_tiled_fn xp_get_encode_tiled() {
 
 static void decide_paths(xp_head* h) {
   h->readout_tc = 0;
+  h->readout_pair_ok = 0;
   h->latent_mma = 0;
   h->hidden_tc = 0;
   int major = 0, minor = 0;
@@ -522,6 +535,13 @@ static void decide_paths(xp_head* h) {
                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS) {
       h->tm_w2 = tm;
       h->readout_tc = 1;
+      const cuuint32_t half[2] = {64, (cuuint32_t)xp_readout_tc_tile() / 2};
+      h->readout_pair_ok =
+          xp_get_encode_tiled()(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, h->w2, dims, strides,
+                                half, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+      if (h->readout_pair_ok) h->tm_w2_half = tm;
     }
   }
 }

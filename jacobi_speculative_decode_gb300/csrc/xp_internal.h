@@ -26,6 +26,9 @@ struct xp_head {
   int readout_tc;        // tcgen05 readout usable for this head's shapes
   int latent_mma;        // cluster tensor-core latent usable for this head's shapes
   CUtensorMap tm_w2;     // W2 [V, r] tiled map for the tcgen05 readout
+  CUtensorMap tm_w2_half;  // the same with half-tile boxes (one CTA of a readout pair)
+  int readout_pair_ok;   // tm_w2_half could be encoded
+  int readout_pairs;     // xp_set_readout_pairs: 2-CTA readout when the row tiles pair up
   CUtensorMap tm_wgu, tm_wd, tm_mixT;  // [w_gate ; w_up] fp16 rows, w_down, mixer slices (TMA)
   void* timeline;        // optional per-CTA per-pass phase timestamps of the persistent refine
   size_t timeline_bytes;
@@ -108,6 +111,8 @@ cudaError_t xp_launch_readout_tc(const xp_head* h, const void* lat, const void* 
                                  int64_t sn, int64_t sb, int N, int64_t* blk, float* win,
                                  unsigned long long* packed, unsigned* ticket, cudaStream_t s);
 int xp_readout_tc_tile();   // vocabulary ids per tile of the tcgen05 readout (w2 map box rows)
+// true when the argmax readout of N blocks runs as 2-CTA pairs (even number of row tiles)
+bool xp_readout_paired(const xp_head* h, int N);
 bool xp_readout_tc_call_ok(const xp_head* h, const void* lat, const void* base, int64_t sn,
                            int64_t sb, int N);
 // logits base + lat.w2 (bias alone when base is null) as fp32 rows of out (row stride ldo)
@@ -125,8 +130,7 @@ size_t xp_persist_xbuf_bytes(int B, int max_N);
 size_t xp_persist_counter_words(int max_N);
 size_t xp_persist_timeline_bytes(const xp_head* h, int K);
 bool xp_persist_call_ok(const xp_head* h, const void* base, int64_t sn, int64_t sb, int N);
-// the automatic choice: at least two row tiles (the latent of one overlaps nothing else
-// otherwise) and one latent round per pass
+// the automatic choice between the persistent and the per-stage passes for N blocks
 bool xp_persist_preferred(const xp_head* h, int N);
 // returns cudaErrorNotSupported (nothing launched) when the call cannot take this path
 cudaError_t xp_launch_persist(const xp_head* h, const void* base, int64_t sn, int64_t sb, int N,

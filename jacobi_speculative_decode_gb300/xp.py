@@ -64,6 +64,8 @@ _SIGS = {
     "xp_jacobi_passes": (_I, [_P, _P, _I64, _I64, _P, _P, _I, _I, _P, _P, _S, _P]),
     "xp_set_pass_mode": (_I, [_P, _I]),
     "xp_passes_persistent": (_I, [_P, _P, _I64, _I64, _I]),
+    "xp_set_readout_pairs": (_I, [_P, _I]),
+    "xp_readout_pairs": (_I, [_P, _I]),
     "xp_get_error": (_I, [_P, _P]),
     "xp_readout_kernel_name": (ctypes.c_char_p, [_P]),
     "xp_profile_timeline": (_I, [_P, _P, _S, _I, ctypes.POINTER(_S)]),
@@ -244,6 +246,14 @@ def xp_set_pass_mode(head, mode: int):
 
 def xp_passes_persistent(head, base, stride_n, stride_b, N) -> bool:
     return bool(lib().xp_passes_persistent(head, _ptr(base), stride_n, stride_b, N))
+
+
+def xp_set_readout_pairs(head, on: bool):
+    _check("xp_set_readout_pairs", lib().xp_set_readout_pairs(head, int(on)))
+
+
+def xp_readout_pairs(head, N) -> bool:
+    return bool(lib().xp_readout_pairs(head, N))
 
 
 def xp_get_error(head, stream=None) -> int:

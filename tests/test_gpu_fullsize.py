@@ -157,6 +157,16 @@ def test_max_batch_readout_all_rows():
     xp.xp_readout_argmax(dev.head.handle, xp.to_device(lat_np, wl.dtype), dev.base, dev.sn,
                          dev.sb, wl.N, blk, win, dev.ws)
     assert xp.xp_get_error(dev.head.handle) == xp.XP_OK
+    # the same readout as 2-CTA pairs (16 clusters of two row tiles x 4 segments)
+    xp.xp_set_readout_pairs(dev.head.handle, True)
+    assert xp.xp_readout_pairs(dev.head.handle, wl.N)
+    blk2 = dev.blk_in.clone()
+    win2 = torch.empty_like(win)
+    xp.xp_readout_argmax(dev.head.handle, xp.to_device(lat_np, wl.dtype), dev.base, dev.sn,
+                         dev.sb, wl.N, blk2, win2, dev.ws)
+    assert xp.xp_get_error(dev.head.handle) == xp.XP_OK
+    assert torch.equal(blk2, blk)
+    assert (win2 - win).abs().max().item() <= 1e-4
     got = blk.cpu().numpy()[:, 1:].reshape(-1)
     got_win = win.cpu().numpy()
     lat = O.decode(lat_np, wl.dtype).reshape(wl.rows, wl.r)
