@@ -514,11 +514,48 @@ bool encode(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* dims,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Co-resident 4-CTA clusters of the argmax kernel, queried once per device.
+constexpr int kMaxDevices = 64;
+template <int KCH>
+int co_resident_clusters4(int device) {
+  constexpr int size = 4;
+  static int cached[kMaxDevices] = {};
+  auto* kern = readout_tc_kernel<KCH, false, false>;
+  const size_t smem = smem_bytes<false, false>();
+  const int d = device >= 0 && device < kMaxDevices ? device : 0;
+  if (cached[d] > 0 && d == device) return cached[d];
+  cudaLaunchConfig_t q = {};
+  q.gridDim = dim3(size);
+  q.blockDim = dim3(NUM_THREADS);
+  q.dynamicSmemBytes = smem;
+  cudaLaunchAttribute a[1];
+  a[0].id = cudaLaunchAttributeClusterDimension;
+  a[0].val.clusterDim.x = size;
+  a[0].val.clusterDim.y = 1;
+  a[0].val.clusterDim.z = 1;
+  q.attrs = a;
+  q.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &q) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    n = 0;
+  }
+  cached[d] = n;
+  return n;
+}
+
 // Row tiles x vocabulary segments, one CTA each: the row tiles are spread over the SMs
 // and every row tile's vocabulary is split into as many segments as there are SMs per
-// row tile.  With an even number of row tiles, neighbouring row tiles of one segment
-// form a 2-CTA cluster that shares its MMAs (block x = segment * n_rt + row tile, so the
-// cluster of blocks 2c, 2c + 1 holds row tiles 2p, 2p + 1 of one segment).
+// row tile (block x = segment * n_rt + row tile).
+// - When the row tiles come in multiples of 4, groups of 4 row tiles of one segment are
+//   launched as 4-CTA clusters, for placement only: the kernel uses no cluster feature,
+//   but a cluster is scheduled inside one GPC, so the CTAs that read the same w2 tiles at
+//   the same time sit together on one die.  At batched decode (4 row tiles) this took
+//   the readout from 44.2 to 40.3 us with the same DRAM bytes; with 8 and 32 row tiles it
+//   was within 1% either way.  The segments are capped so that every cluster is resident
+//   at once (36 clusters of 4 at this shared-memory size: 144 CTAs).
+// - PAIR: neighbouring row tiles of one segment form a 2-CTA cluster that shares its MMAs
+//   (the cluster of blocks 2c, 2c + 1 holds row tiles 2p, 2p + 1 of one segment).
 template <int KCH, bool PAIR>
 cudaError_t launch_argmax(const xp_head* h, const void* lat, const CUtensorMap& tb, int N,
                           int64_t* blk, float* win, unsigned long long* packed,
@@ -527,12 +564,20 @@ cudaError_t launch_argmax(const xp_head* h, const void* lat, const CUtensorMap& 
   const int bpt = BM / Bm1, rpt = bpt * Bm1;
   const int n_rt = (N + bpt - 1) / bpt;
   const int nvt = (h->V + BN - 1) / BN;
-  const int n_seg = std::max(1, std::min(nvt, h->num_sms / n_rt));
+  int n_seg = std::max(1, std::min(nvt, h->num_sms / n_rt));
   const size_t smem = smem_bytes<false, PAIR>();
   auto* kern = readout_tc_kernel<KCH, false, PAIR>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
+  int cluster = PAIR ? 2 : 1;
+  if (!PAIR && n_rt % 4 == 0) {
+    const int mc = co_resident_clusters4<KCH>(h->device);
+    if (mc * 4 >= n_rt) {
+      cluster = 4;
+      n_seg = std::max(1, std::min(n_seg, mc * 4 / n_rt));
+    }
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(n_rt * n_seg);
   cfg.blockDim = dim3(NUM_THREADS);
@@ -542,11 +587,11 @@ cudaError_t launch_argmax(const xp_head* h, const void* lat, const CUtensorMap& 
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   attr[1].id = cudaLaunchAttributeClusterDimension;
-  attr[1].val.clusterDim.x = 2;
+  attr[1].val.clusterDim.x = cluster;
   attr[1].val.clusterDim.y = 1;
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = PAIR ? 2 : 1;
+  cfg.numAttrs = cluster > 1 ? 2 : 1;
   e = cudaLaunchKernelEx(&cfg, kern, (const __nv_bfloat16*)lat, PAIR ? h->tm_w2_half : h->tm_w2,
                          tb, rows, Bm1, h->B, h->V, rpt, bpt, n_rt, n_seg, nvt, blk, win,
                          h->latent_mma ? (const float*)h->E : (const float*)nullptr, h->r * 4,
