@@ -333,6 +333,37 @@ def other_workloads(args):
              "rows_per_s": round(wl.K * wl.rows / (ms / 1e3), 1),
              "config": {"N": wl.N, "B": wl.B, "V": wl.V, "hidden": wl.hidden, "K": wl.K,
                         "topc": wl.topc}}
+        if not wl.topc:
+            r["roofline_step_frac"] = round(pass_bytes(wl) * wl.K / (ms / 1e3) / 1e9 / hbm, 4)
+            # the latent's share of a pass, from the single-pass entry points chained as in a step
+            xh = torch.empty(wl.N, wl.B, wl.r, dtype=torch.float32, device="cuda")
+            lat = torch.empty(wl.N, wl.B - 1, wl.r, dtype=xp.torch_dtype(wl.dtype), device="cuda")
+            xp.xp_hidden_cache(head.handle, h, wl.N, xh, ws)
+            xp.xp_init_argmax(head.handle, base, sn, sb, anchor, wl.N, blk, None, ws)
+
+            def chained_us(fn, n=30):
+                for _ in range(3):
+                    fn()
+                c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                c0.record(stream)
+                for _ in range(n):
+                    fn()
+                c1.record(stream)
+                torch.cuda.synchronize()
+                return c0.elapsed_time(c1) / n * 1e3
+
+            def readout():
+                xp.xp_readout_argmax(head.handle, lat, base, sn, sb, wl.N, blk, None, ws)
+
+            def one_pass():
+                xp.xp_latent_pass(head.handle, blk, am1, xh, wl.N, lat)
+                readout()
+
+            ro_us, pass_us = chained_us(readout), chained_us(one_pass)
+            r["readout_us"] = round(ro_us, 2)
+            r["pass_us"] = round(pass_us, 2)
+            r["latent_share_of_pass"] = round(max(pass_us - ro_us, 0.0) / pass_us, 4)
+            del xh, lat
         if xp.xp_get_error(head.handle) != xp.XP_OK:
             r["device_error"] = True
         if wl.topc:
