@@ -35,6 +35,8 @@
 // per-stage and per-tile signals carry no fence (a fenced remote arrive costs a memory
 // barrier each, and the forwarding thread would serialise on them): what they report --
 // a TMA copy seen complete, tensor-memory reads waited for -- is already ordered.
+// Pairs are off unless the caller asks for them: the vocabulary loop is bound by the
+// streams from HBM, and on GB300 the pair was not faster than one CTA per row tile.
 //
 // Every base stage is consumed by one fixed group of four warps (the ring size is a
 // multiple of the thirds per tile), and a group consumes its stages in order, so no
